@@ -1,0 +1,189 @@
+/*
+ * pkv.h — C ABI of the GB300 paged KV-cache decode library (libpkv.so).
+ *
+ * What the library computes, and where the reference pages state it:
+ *   - "KV Cache는 왜 LLM 서빙의 핵심인가", section "KV Cache: O(T²)를 O(T)로"
+ *     (decode-step listing): each step appends the new token's k_t, v_t to the
+ *     cache and computes softmax(q_t K^T / sqrt(d)) V over the whole cache.
+ *   - "LLM 서빙과 KV Cache, VLLM", section "PagedAttention": the cache is cut
+ *     into fixed-size token blocks that live anywhere in one shared pool.
+ *   - "KV Cache는 왜 LLM 서빙의 핵심인가", section "메모리 공식과 GQA의 동기",
+ *     and "KV 캐시 시스템 (KV Cache System)", section "MQA / GQA": n_h query
+ *     heads share n_kv K/V groups; MHA is n_kv = n_h, MQA is n_kv = 1.
+ *   - "KV Cache는 왜 LLM 서빙의 핵심인가", section "KVQuant: 마지막 4배": INT4
+ *     K per channel, V per token, step size (max - min) / (2^4 - 1).
+ *   - "Research Paper Review : CACHE BLEND ...", section "Background": reused
+ *     chunks are brought to their real position by one extra RoPE rotation of
+ *     their keys by (real start - 0).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory and frees nothing; scratch space is passed in
+ *     (`workspace`).  Tensors are dense, row-major, in the layouts stated below.
+ *   - bf16 / fp16 tensors are passed as `void*` (2-byte elements).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     only enqueues work on `stream` and returns; the caller orders calls (e.g.
+ *     append before attend) by issuing them on one stream.
+ *   - Argument errors are returned synchronously as a negative pkv_status and
+ *     nothing is enqueued.  Errors only the GPU can see (a block-table entry or
+ *     slot out of range, a context length out of range, a bounded wait that gave
+ *     up) set bits in `*err_flag` (a caller-owned device int32, may be NULL): the
+ *     offending item is skipped (its block contributes nothing / the token is
+ *     not written) and no access goes out of bounds.  The caller clears the flag.
+ *   - Pool layout (bf16): [num_blocks][n_kv][block_size][head_dim]; the tile of
+ *     one (block, kv head) is contiguous.
+ *   - Supported: head_dim in {64, 128}; block_size in {16, 32, 64};
+ *     n_h % n_kv == 0 with group n_h / n_kv <= 64.  Other values give PKV_EINVAL.
+ *     q, out, pools, codes and workspace must be 16-byte aligned.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,   /* bad argument: shape, null pointer, alignment, unsupported size */
+  PKV_ERANGE = -2,   /* a size beyond a documented maximum */
+  PKV_ECUDA = -3,    /* a CUDA call failed (no device, launch error); see pkv_last_cuda_error() */
+  PKV_ENOSPC = -4    /* workspace smaller than pkv_decode_workspace_bytes() */
+} pkv_status;
+
+/* Bits ORed into *err_flag by the kernels. */
+#define PKV_DEV_BAD_BLOCK 1  /* block_tables entry outside [0, num_blocks): block skipped   */
+#define PKV_DEV_BAD_SLOT  2  /* slot >= num_blocks * block_size (or bad tail row): skipped  */
+#define PKV_DEV_BAD_CTX   4  /* context_lens[s] < 0 or > max_blocks * block_size: clamped  */
+#define PKV_DEV_TIMEOUT   8  /* a bounded wait inside a kernel gave up (about 2 s)          */
+
+/* Output element types of the attention calls. */
+#define PKV_OUT_BF16 0
+#define PKV_OUT_F32  1
+
+/* Human-readable name of a status. */
+const char* pkv_status_str(int status);
+/* The last CUDA error code seen by the library on this thread (cudaError_t as int). */
+int pkv_last_cuda_error(void);
+
+/*
+ * kv_append — write each new token's K and V rows into the pools at its slot.
+ * Decode-step listing, "append" line (see file header).
+ *   k, v          bf16 [n_tok][n_kv][head_dim]
+ *   slot_mapping  int64 [n_tok]; slot = physical block * block_size + row.
+ *                 A negative slot is padding and is skipped.  Slots must be distinct.
+ *   k_pool,v_pool bf16 [num_blocks][n_kv][block_size][head_dim], updated in place.
+ * Bit-exact copy.  A slot >= num_blocks * block_size sets PKV_DEV_BAD_SLOT.
+ */
+pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int n_tok,
+                         void* k_pool, void* v_pool, int num_blocks, int block_size, int n_kv,
+                         int head_dim, int32_t* err_flag, void* stream);
+
+/*
+ * Bytes of workspace pkv_paged_decode_attn (int4 = 0) or pkv_paged_decode_attn_int4
+ * (int4 = 1) needs for this shape on the current device.  0 on an invalid shape.
+ */
+size_t pkv_decode_workspace_bytes(int batch, int n_h, int n_kv, int head_dim, int block_size, int int4);
+
+/*
+ * paged_decode_attn — one decode step of attention over a paged bf16 cache.
+ * Decode-step listing, attention line; PagedAttention blocks; GQA groups.
+ *   q             bf16 [batch][n_h][head_dim]
+ *   k_pool,v_pool bf16 [num_blocks][n_kv][block_size][head_dim]
+ *   block_tables  int32 [batch][max_blocks]; entry i of row s is the physical block
+ *                 holding tokens [i*block_size, (i+1)*block_size) of sequence s.
+ *                 Entries past ceil(context_lens[s] / block_size) are not read.
+ *   context_lens  int32 [batch]; tokens of sequence s, including the one appended
+ *                 this step.  0 gives a zero output row.
+ *   scale         multiplies q.k before the softmax (1/sqrt(head_dim) for the usual layer)
+ *   out           [batch][n_h][head_dim], bf16 (out_dtype PKV_OUT_BF16, round to
+ *                 nearest even) or fp32 (PKV_OUT_F32)
+ *   workspace     device scratch of at least pkv_decode_workspace_bytes(..., 0) bytes,
+ *                 256-byte aligned; its contents on entry do not matter.
+ * Arithmetic: q.k and p.v products in fp32 (tensor-core mma, bf16 inputs, fp32
+ * accumulate; p is carried as a bf16 high + low pair), softmax online in fp32.
+ * The result depends only on the logical token order, never on which physical
+ * blocks hold the tokens.
+ */
+pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_tables, int max_blocks,
+                                 const int32_t* context_lens, float scale, int batch, int n_h,
+                                 int n_kv, int head_dim, int block_size, int num_blocks,
+                                 void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                                 int32_t* err_flag, void* stream);
+
+/*
+ * kv_quant_append_int4 — quantize-on-append into an INT4 paged cache.
+ * "KVQuant: 마지막 4배": K per channel, V per token, s = (max - min) / 15.
+ * Exact op sequence (codes are bit-exact against it):
+ *   lo, hi = fp32 min / max of the group (a zero lo is taken as +0);
+ *   s32 = (hi - lo) / 15 (fp32, nearest);
+ *   s16 = fp16(s32), m16 = fp16(lo) (nearest even);
+ *   code = clamp(rint_half_even((x - m16) / s16), 0, 15) (fp32 subtract / divide),
+ *   code = 0 when s16 == 0; dequantized x^ = code * s16 + m16.
+ * Groups: V = the head_dim channels of one (token, kv head); K = one channel of one
+ * (block, kv head) over the block's block_size rows.  K rows of a block that is not
+ * yet full stay in bf16 in `k_tail`; when a call appends a block's last row, the
+ * whole block is quantized from the rows appended earlier in the same call and the
+ * tail rows, and the tail is left as it was.
+ *   k, v          bf16 [n_tok][n_kv][head_dim]
+ *   slot_mapping  int64 [n_tok] (negative = padding); tail_seq int32 [n_tok]: the
+ *                 tail row (batch index) of each token's sequence, in [0, tail_rows).
+ *   k_codes, v_codes  uint8 [num_blocks][n_kv][block_size][head_dim/2]: 8 channels
+ *                 per little-endian 32-bit word, nibble n of word w holds channel
+ *                 8w + (0,2,4,6,1,3,5,7)[n] (even channels in the low half-word).
+ *   k_meta        fp16 [num_blocks][n_kv][2][head_dim]: scale row, then min row.
+ *   v_meta        fp16 [num_blocks][n_kv][block_size][2]: (scale, min) per token.
+ *   k_tail        bf16 [tail_rows][n_kv][block_size][head_dim].
+ * Caller contract: slots distinct; within one call the tokens of a sequence are
+ * consecutive entries in logical order with one tail_seq; a sequence starts at
+ * row 0 of its first block.  Values must lie within fp16 range.
+ * Enqueues two kernels (quantize, then tail update) on `stream`.
+ */
+pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, const int64_t* slot_mapping,
+                                    const int32_t* tail_seq, int n_tok, uint8_t* k_codes,
+                                    void* k_meta, uint8_t* v_codes, void* v_meta, void* k_tail,
+                                    int tail_rows, int num_blocks, int block_size, int n_kv,
+                                    int head_dim, int32_t* err_flag, void* stream);
+
+/*
+ * paged_decode_attn_int4 — decode attention over the INT4 cache written by
+ * pkv_kv_quant_append_int4.  Full blocks are dequantized in registers (K and V
+ * to fp16, x^ = code * s + m); the last, unfinished block of sequence s takes
+ * its K rows from k_tail[s] (bf16) and its V rows from the codes.
+ * Same arguments and output as pkv_paged_decode_attn, with the INT4 tensors in
+ * place of the pools; the batch index is the tail row.  q.k and p.v use fp16
+ * tensor-core mma with fp32 accumulation.
+ */
+pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, const void* k_meta,
+                                      const uint8_t* v_codes, const void* v_meta,
+                                      const void* k_tail, const int32_t* block_tables,
+                                      int max_blocks, const int32_t* context_lens, float scale,
+                                      int batch, int n_h, int n_kv, int head_dim, int block_size,
+                                      int num_blocks, void* out, int out_dtype, void* workspace,
+                                      size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
+ * rope_shift_k — re-rotate the keys of reused chunks in place.
+ * "Research Paper Review : CACHE BLEND ...", section "Background" (full KV reuse).
+ * Every row and kv head of block block_ids[i] is rotated by position deltas[i]:
+ * channel pairs (j, j + head_dim/2), angle deltas[i] * rope_base^(-2j/head_dim),
+ *   x_j' = x_j cos - x_{j+d/2} sin,  x_{j+d/2}' = x_j sin + x_{j+d/2} cos,
+ * angle reduced in fp64, rotation in fp32, stored bf16 (nearest even).
+ * A delta of 0 leaves the block untouched.  block_ids must be distinct; an id
+ * outside [0, num_blocks) sets PKV_DEV_BAD_BLOCK and is skipped.
+ *   k_pool   bf16 [num_blocks][n_kv][block_size][head_dim]
+ *   block_ids, deltas  int32 [n_blocks]
+ */
+pkv_status pkv_rope_shift_k(void* k_pool, const int32_t* block_ids, const int32_t* deltas,
+                            int n_blocks, int num_blocks, int n_kv, int block_size, int head_dim,
+                            double rope_base, int32_t* err_flag, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -32,7 +32,7 @@ from .rounding import round_bf16, round_fp16_from_f32
 from .paged_attention import (kv_append, gather_sequence, paged_decode_attention,
                               attention_weights)
 from .kv_sizes import kv_bytes, kv_bytes_gqa, kv_bytes_per_token
-from .int4 import (quantize_group, pack_codes, unpack_codes, Int4Cache,
+from .int4 import (quantize_group, quantize_groups, pack_codes, unpack_codes, Int4Cache,
                    paged_decode_attention_int4)
 from .rope import rope_shift_k, rotate
 from .brute import attention_loops
@@ -40,6 +40,6 @@ from .brute import attention_loops
 __all__ = [
     "round_bf16", "round_fp16_from_f32", "kv_append", "gather_sequence",
     "paged_decode_attention", "attention_weights", "kv_bytes", "kv_bytes_gqa",
-    "kv_bytes_per_token", "quantize_group", "pack_codes", "unpack_codes", "Int4Cache",
+    "kv_bytes_per_token", "quantize_group", "quantize_groups", "pack_codes", "unpack_codes", "Int4Cache",
     "paged_decode_attention_int4", "rope_shift_k", "rotate", "attention_loops",
 ]

@@ -11,7 +11,8 @@ Readings of what the page leaves open (each one is also a line of the design not
   max - min, so the codes would not fit 0..15.  Reading: asymmetric codes
   against the group minimum, code = round((x - min) / s), x^ = code * s + min.
 * Precision of each step (fixed so that codes are bit-exact by construction):
-  (1) lo, hi = float32 min / max of the group (exact for bf16 inputs);
+  (1) lo, hi = float32 min / max of the group (exact for bf16 inputs); a zero
+      minimum is taken as +0 (so the stored fp16 min never depends on the sign of zero);
   (2) s32 = (hi - lo) / 15 in float32, round to nearest;
   (3) s16 = fp16(s32), m16 = fp16(lo), both round to nearest even;
   (4) code = clamp(rint_half_even((x - m16) / s16), 0, 15) with float32
@@ -38,7 +39,7 @@ NIBBLE_CHANNEL = (0, 2, 4, 6, 1, 3, 5, 7)
 def quantize_group(x) -> tuple:
     """Codes (uint8 0..15), fp16 scale and fp16 min of one group, steps (1)-(4) above."""
     x = np.asarray(x, dtype=np.float32)
-    lo = np.float32(x.min())
+    lo = np.float32(np.float32(x.min()) + np.float32(0.0))     # -0 + 0 = +0
     hi = np.float32(x.max())
     s32 = np.float32(np.float32(hi - lo) / np.float32(15.0))
     s16 = np.float16(s32)
@@ -49,6 +50,25 @@ def quantize_group(x) -> tuple:
         return np.zeros(x.shape, dtype=np.uint8), s16, m16
     q = np.rint((x - m) / s)
     return np.clip(q, 0, 15).astype(np.uint8), s16, m16
+
+
+def quantize_groups(x) -> tuple:
+    """quantize_group applied to every group along the last axis at once (same op sequence).
+
+    x: float32 [..., n] -> codes uint8 [..., n], s16 float16 [...], m16 float16 [...].
+    """
+    x = np.asarray(x, dtype=np.float32)
+    lo = (x.min(axis=-1) + np.float32(0.0)).astype(np.float32)
+    hi = x.max(axis=-1)
+    s32 = ((hi - lo) / np.float32(15.0)).astype(np.float32)
+    s16 = s32.astype(np.float16)
+    m16 = lo.astype(np.float16)
+    s = s16.astype(np.float32)[..., None]
+    m = m16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint((x - m) / s)
+    q = np.where(s == 0, 0, np.clip(q, 0, 15))
+    return q.astype(np.uint8), s16, m16
 
 
 def dequantize(codes, s16, m16):
@@ -111,27 +131,29 @@ class Int4Cache:
             if slot < 0:
                 continue
             blk, row = divmod(slot, bs)
-            for g in range(n_kv):                                   # V: per token
-                codes, s16, m16 = quantize_group(v[i, g])
-                self.v_codes[blk, g, row] = pack_codes(codes)
-                self.v_meta[blk, g, row] = (s16, m16)
+            codes, s16, m16 = quantize_groups(v[i])               # V: per token, every kv head
+            self.v_codes[blk, :, row] = pack_codes(codes)
+            self.v_meta[blk, :, row, 0] = s16
+            self.v_meta[blk, :, row, 1] = m16
             if row == bs - 1:
                 completed.add((tails[i], blk))
+        latest = {}                                                 # (seq, slot) -> latest in-call token
         for i, slot in enumerate(slots):                            # K: whole blocks
-            if slot < 0 or slot % bs != bs - 1:
+            if slot < 0:
+                continue
+            latest[(tails[i], slot)] = i
+            if slot % bs != bs - 1:
                 continue
             blk, seq = slot // bs, tails[i]
             rows = self.k_tail[seq].copy()                          # rows not in this call
-            for j in range(i + 1):
-                if slots[j] >= 0 and slots[j] // bs == blk and tails[j] == seq:
-                    rows[:, slots[j] % bs] = k[j]
-            for g in range(n_kv):
-                codes = np.zeros((bs, self.D), np.uint8)
-                for c in range(self.D):
-                    codes[:, c], s16, m16 = quantize_group(rows[g, :, c])
-                    self.k_meta[blk, g, 0, c] = s16
-                    self.k_meta[blk, g, 1, c] = m16
-                self.k_codes[blk, g] = pack_codes(codes)
+            for r in range(bs):
+                j = latest.get((seq, blk * bs + r))
+                if j is not None:
+                    rows[:, r] = k[j]
+            codes, s16, m16 = quantize_groups(rows.transpose(0, 2, 1))   # [n_kv][D] groups of bs rows
+            self.k_meta[blk, :, 0] = s16
+            self.k_meta[blk, :, 1] = m16
+            self.k_codes[blk] = pack_codes(codes.transpose(0, 2, 1))
         for i, slot in enumerate(slots):                            # K tail of unfinished blocks
             if slot < 0:
                 continue

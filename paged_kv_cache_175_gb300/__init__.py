@@ -1,0 +1,198 @@
+"""Python binding of libpkv.so — paged KV-cache decode attention for GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA library
+(see include/pkv.h for the contract of each call).  torch supplies device memory
+and streams.  There is no CPU fallback: the calls raise if the library is not
+built or a tensor is not on a CUDA device.
+
+Functions (same names as the C entry points without the ``pkv_`` prefix):
+``kv_append``, ``paged_decode_attn``, ``kv_quant_append_int4``,
+``paged_decode_attn_int4``, ``rope_shift_k``, plus ``decode_workspace_bytes`` and
+``alloc_int4_cache``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from ._build import LIB as LIB_PATH, build_library
+
+PKV_OUT_BF16 = 0
+PKV_OUT_F32 = 1
+DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_CTX, DEV_TIMEOUT = 1, 2, 4, 8
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "pkv_status_str": (ctypes.c_char_p, [_I]),
+    "pkv_last_cuda_error": (_I, []),
+    "pkv_kv_append": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "pkv_paged_decode_attn": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
+                                   _P, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pkv_kv_quant_append_int4": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pkv_paged_decode_attn_int4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I,
+                                        _I, _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pkv_rope_shift_k": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_double, _P, _P]),
+}
+
+
+class PkvError(RuntimeError):
+    pass
+
+
+def lib(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libpkv.so (fails loudly if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            if not build_if_missing:
+                raise PkvError(f"{LIB_PATH} is missing: build it with paged_kv_cache_175_gb300._build.build_library()")
+            build_library()
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(name: str, status: int):
+    if status != 0:
+        msg = lib().pkv_status_str(status).decode()
+        extra = f" (cuda error {lib().pkv_last_cuda_error()})" if status == -3 else ""
+        raise PkvError(f"{name}: {msg}{extra}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise PkvError("tensors must be contiguous CUDA tensors")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def kv_append(k, v, slot_mapping, k_pool, v_pool, err=None, stream=None):
+    """Write k, v [n_tok][n_kv][d] (bf16) into the pools at slot_mapping (int64)."""
+    _cuda(k, v, slot_mapping, k_pool, v_pool, err)
+    assert k.dtype == v.dtype == k_pool.dtype == v_pool.dtype == torch.bfloat16
+    assert slot_mapping.dtype == torch.int64
+    num_blocks, n_kv, bs, d = k_pool.shape
+    _check("kv_append", lib().pkv_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], _ptr(k_pool),
+                                            _ptr(v_pool), num_blocks, bs, n_kv, d, _ptr(err), _stream(stream)))
+
+
+def decode_workspace_bytes(batch, n_h, n_kv, head_dim, block_size, int4=False) -> int:
+    n = lib().pkv_decode_workspace_bytes(batch, n_h, n_kv, head_dim, block_size, 1 if int4 else 0)
+    if n == 0 and batch > 0:
+        raise PkvError("decode_workspace_bytes: invalid shape or no device")
+    return n
+
+
+def _workspace(nbytes, device):
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _out(q, out, out_dtype):
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    assert out.shape == q.shape and out.dtype in (torch.bfloat16, torch.float32)
+    return out, (PKV_OUT_F32 if out.dtype == torch.float32 else PKV_OUT_BF16)
+
+
+def paged_decode_attn(q, k_pool, v_pool, block_tables, context_lens, scale, out=None, out_dtype=torch.bfloat16,
+                      workspace=None, err=None, stream=None):
+    """Decode attention over a paged bf16 cache; returns out [B][n_h][d]."""
+    _cuda(q, k_pool, v_pool, block_tables, context_lens, out, workspace, err)
+    assert q.dtype == k_pool.dtype == v_pool.dtype == torch.bfloat16
+    assert block_tables.dtype == context_lens.dtype == torch.int32
+    B, n_h, d = q.shape
+    num_blocks, n_kv, bs, d2 = k_pool.shape
+    assert d2 == d and v_pool.shape == k_pool.shape
+    out, od = _out(q, out, out_dtype)
+    need = decode_workspace_bytes(B, n_h, n_kv, d, bs)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    _check("paged_decode_attn", lib().pkv_paged_decode_attn(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        float(scale), B, n_h, n_kv, d, bs, num_blocks, _ptr(out), od, _ptr(workspace), workspace.numel(),
+        _ptr(err), _stream(stream)))
+    return out
+
+
+@dataclass
+class Int4CacheTensors:
+    k_codes: torch.Tensor     # uint8 [num_blocks][n_kv][bs][d/2]
+    k_meta: torch.Tensor      # fp16  [num_blocks][n_kv][2][d]
+    v_codes: torch.Tensor     # uint8 [num_blocks][n_kv][bs][d/2]
+    v_meta: torch.Tensor      # fp16  [num_blocks][n_kv][bs][2]
+    k_tail: torch.Tensor      # bf16  [tail_rows][n_kv][bs][d]
+
+    @property
+    def shape(self):
+        nb, n_kv, bs, dh = self.k_codes.shape
+        return nb, n_kv, bs, dh * 2
+
+
+def alloc_int4_cache(num_blocks, n_kv, block_size, head_dim, tail_rows, device="cuda") -> Int4CacheTensors:
+    z = dict(device=device)
+    return Int4CacheTensors(
+        torch.zeros(num_blocks, n_kv, block_size, head_dim // 2, dtype=torch.uint8, **z),
+        torch.zeros(num_blocks, n_kv, 2, head_dim, dtype=torch.float16, **z),
+        torch.zeros(num_blocks, n_kv, block_size, head_dim // 2, dtype=torch.uint8, **z),
+        torch.zeros(num_blocks, n_kv, block_size, 2, dtype=torch.float16, **z),
+        torch.zeros(tail_rows, n_kv, block_size, head_dim, dtype=torch.bfloat16, **z))
+
+
+def kv_quant_append_int4(k, v, slot_mapping, tail_seq, cache: Int4CacheTensors, err=None, stream=None):
+    """Quantize-on-append of k, v [n_tok][n_kv][d] into the INT4 cache."""
+    _cuda(k, v, slot_mapping, tail_seq, cache.k_codes, cache.k_meta, cache.v_codes, cache.v_meta, cache.k_tail, err)
+    assert k.dtype == v.dtype == torch.bfloat16 and slot_mapping.dtype == torch.int64
+    assert tail_seq.dtype == torch.int32
+    nb, n_kv, bs, d = cache.shape
+    _check("kv_quant_append_int4", lib().pkv_kv_quant_append_int4(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(tail_seq), k.shape[0], _ptr(cache.k_codes), _ptr(cache.k_meta),
+        _ptr(cache.v_codes), _ptr(cache.v_meta), _ptr(cache.k_tail), cache.k_tail.shape[0], nb, bs, n_kv, d,
+        _ptr(err), _stream(stream)))
+
+
+def paged_decode_attn_int4(q, cache: Int4CacheTensors, block_tables, context_lens, scale, out=None,
+                           out_dtype=torch.bfloat16, workspace=None, err=None, stream=None):
+    """Decode attention over the INT4 cache; the batch index is the tail row."""
+    _cuda(q, block_tables, context_lens, out, workspace, err)
+    assert q.dtype == torch.bfloat16
+    B, n_h, d = q.shape
+    nb, n_kv, bs, d2 = cache.shape
+    assert d2 == d and cache.k_tail.shape[0] >= B
+    out, od = _out(q, out, out_dtype)
+    need = decode_workspace_bytes(B, n_h, n_kv, d, bs, int4=True)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    _check("paged_decode_attn_int4", lib().pkv_paged_decode_attn_int4(
+        _ptr(q), _ptr(cache.k_codes), _ptr(cache.k_meta), _ptr(cache.v_codes), _ptr(cache.v_meta),
+        _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), B, n_h,
+        n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
+    return out
+
+
+def rope_shift_k(k_pool, block_ids, deltas, rope_base=10000.0, err=None, stream=None):
+    """Rotate every key of block block_ids[i] by position deltas[i] in place."""
+    _cuda(k_pool, block_ids, deltas, err)
+    assert k_pool.dtype == torch.bfloat16 and block_ids.dtype == deltas.dtype == torch.int32
+    num_blocks, n_kv, bs, d = k_pool.shape
+    _check("rope_shift_k", lib().pkv_rope_shift_k(_ptr(k_pool), _ptr(block_ids), _ptr(deltas), block_ids.numel(),
+                                                  num_blocks, n_kv, bs, d, float(rope_base), _ptr(err),
+                                                  _stream(stream)))

@@ -1,0 +1,115 @@
+// Work partition shared by the paged decode-attention kernels.
+//
+// The unit of work is one (sequence s, kv head g, logical block i) triple.  All units
+// are laid out on one line in (s, g, i) order: sequence s with nb_s = ceil(ctx_s / bs)
+// blocks owns positions [n_kv * cum[s], n_kv * cum[s+1]) where cum is the exclusive
+// prefix sum of nb; inside it, kv head g owns the segment starting at
+// n_kv * cum[s] + g * nb_s.  The line of W = n_kv * cum[B] positions is cut into P
+// equal pieces, piece p = [floor(p W / P), floor((p+1) W / P)), one per CTA of a
+// persistent grid, so every CTA streams the same number of K/V tiles whatever the
+// mix of context lengths.  A segment cut by piece boundaries leaves one partial
+// softmax state per piece it touches, stored at part index (segment + piece), which
+// is unique because both indices grow along the line; the reduce kernel merges them.
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_VALID = 8 };
+
+struct DecodeArgs {
+  const void* q;                 // bf16 [B][n_h][D]
+  const int32_t* bt;             // [B][max_blocks]
+  int max_blocks;
+  const int32_t* cum;            // workspace: [B+1] exclusive prefix of blocks per sequence
+  const int32_t* ctx_eff;        // workspace: [B] context lengths after range checks
+  int batch, n_h, n_kv, G, num_blocks;
+  float scale_log2;              // scale * log2(e): softmax runs in base 2
+  void* out;
+  int out_f32;
+  float* ws_ml;                  // [parts][G][2] (running max in log2 units, running sum)
+  float* ws_o;                   // [parts][G][D] unnormalised partial outputs
+  int32_t* err;
+  int stages;
+  // INT4 cache (unused by the bf16 kernel)
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  const __half* k_meta;
+  const __half* v_meta;
+  const __nv_bfloat16* k_tail;
+};
+
+struct WorkspaceLayout {
+  size_t cum, ctx, ml, o, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ inline WorkspaceLayout workspace_layout(int B, int n_kv, int G, int D, int P) {
+  WorkspaceLayout w;
+  const size_t parts = (size_t)B * n_kv + (size_t)P;
+  w.cum = 0;
+  w.ctx = align_up(sizeof(int32_t) * (size_t)(B + 1), 16);
+  w.ml = align_up(w.ctx + sizeof(int32_t) * (size_t)B, 256);
+  w.o = align_up(w.ml + sizeof(float) * parts * G * 2, 256);
+  w.total = align_up(w.o + sizeof(float) * parts * G * D, 256);
+  return w;
+}
+
+// Piece that holds line position pos (the largest p with floor(p W / P) <= pos).
+__device__ __forceinline__ int piece_of(long long pos, long long W, int P) {
+  return (int)(((pos + 1) * (long long)P - 1) / W);
+}
+
+// Warp-uniform cursor over the line of positions.
+struct Cursor {
+  int s, g, blk, nb, ctx;
+  long long seg_start;           // line position of block 0 of segment (s, g)
+};
+
+__device__ __forceinline__ void cursor_init(Cursor& c, long long pos, const DecodeArgs& a) {
+  int lo = 0, hi = a.batch - 1;
+  while (lo < hi) {                                  // largest s with n_kv * cum[s] <= pos
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)a.n_kv * a.cum[mid] <= pos) lo = mid; else hi = mid - 1;
+  }
+  c.s = lo;
+  c.nb = a.cum[lo + 1] - a.cum[lo];
+  c.ctx = a.ctx_eff[lo];
+  const long long off = pos - (long long)a.n_kv * a.cum[lo];
+  c.g = (int)(off / c.nb);
+  c.blk = (int)(off % c.nb);
+  c.seg_start = pos - c.blk;
+}
+
+// Advance by one position; only called while positions remain, so a non-empty
+// sequence lies ahead when the kv heads of the current one are exhausted.
+__device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
+  if (++c.blk < c.nb) return;
+  c.seg_start += c.nb;
+  c.blk = 0;
+  if (++c.g < a.n_kv) return;
+  c.g = 0;
+  do {
+    ++c.s;
+    c.nb = a.cum[c.s + 1] - a.cum[c.s];
+  } while (c.nb == 0 && c.s < a.batch - 1);
+  c.ctx = a.ctx_eff[c.s];
+}
+
+// Host launchers (decode_plan.cu).
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,
+                        const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream);
+cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void** args);
+int device_sm_count();
+int mt_for_group(int G);           // consumer warps (16 heads each) per CTA
+int bf16_pieces(int D, int BS, int G);
+int int4_pieces(int D, int BS, int G);
+void record_cuda_error(cudaError_t e);
+int encode_tensor_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1);
+
+}  // namespace pkv

@@ -1,0 +1,200 @@
+// Plan and split-reduce kernels of the paged decode attention, plus host utilities
+// shared by every entry point (error bookkeeping, SM count, tensor-map encoding,
+// programmatic-dependent launches).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "decode_common.cuh"
+
+namespace pkv {
+
+static thread_local int g_last_cuda_error = 0;
+
+void record_cuda_error(cudaError_t e) {
+  if (e != cudaSuccess) g_last_cuda_error = (int)e;
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int encode_tensor_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return -1;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                      elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
+cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+// ---- plan: range-check context lengths and scan blocks per sequence ---------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ ctx, int batch, int max_ctx,
+                                                    int block_size, int32_t* __restrict__ cum,
+                                                    int32_t* __restrict__ ctx_eff, int32_t* err) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < batch; base += 1024) {
+    const int s = base + threadIdx.x;
+    int nb = 0;
+    if (s < batch) {
+      int c = ctx[s];
+      if (c < 0 || c > max_ctx) {
+        set_err(err, PKV_DEV_BAD_CTX);
+        c = c < 0 ? 0 : max_ctx;
+      }
+      ctx_eff[s] = c;
+      nb = (c + block_size - 1) / block_size;
+    }
+    int x = nb;                                               // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL_MASK, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int excl = carry + (warp ? warp_sums[warp - 1] : 0) + x - nb;
+    if (s < batch) cum[s] = excl;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = excl + nb;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) cum[batch] = carry;
+}
+
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,
+                        const DecodeArgs& a, cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(context_lens, batch, max_ctx, block_size,
+                                      const_cast<int32_t*>(a.cum), const_cast<int32_t*>(a.ctx_eff), a.err);
+  return cudaGetLastError();
+}
+
+// ---- reduce: merge the partial softmax states of segments split across pieces ----------------
+// One warp per (sequence, q head).  Segments that fit in one piece were finished by the
+// attention kernel itself; empty sequences get a zero row here.
+template <int D>
+__global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) {
+  grid_dep_wait();
+  constexpr int V = D / 32;                                   // channels per lane
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= a.batch * a.n_h) return;
+  const int s = row / a.n_h, h = row % a.n_h, g = h / a.G, hl = h % a.G;
+  const int c0 = a.cum[s], nb = a.cum[s + 1] - c0;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  if (nb > 0) {
+    const long long W = (long long)a.n_kv * a.cum[a.batch];
+    const long long seg_start = (long long)a.n_kv * c0 + (long long)g * nb;
+    const int p0 = piece_of(seg_start, W, P), p1 = piece_of(seg_start + nb - 1, W, P);
+    if (p0 == p1) return;
+    const long long seg = (long long)s * a.n_kv + g;
+    float M = -INFINITY;
+    for (int p = p0; p <= p1; ++p) M = fmaxf(M, a.ws_ml[((seg + p) * a.G + hl) * 2]);
+    float L = 0.f;
+    for (int p = p0; p <= p1; ++p) {
+      const long long part = (seg + p) * a.G + hl;
+      const float w = ex2(a.ws_ml[part * 2] - M);
+      L += w * a.ws_ml[part * 2 + 1];
+      const float* src = a.ws_o + part * D + lane * V;
+      if constexpr (V == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x; acc[1] += w * v.y;
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] *= inv;
+  }
+  const size_t o = (size_t)row * D + lane * V;
+  if (a.out_f32) {
+    float* out = reinterpret_cast<float*>(a.out) + o;
+#pragma unroll
+    for (int i = 0; i < V; ++i) out[i] = acc[i];
+  } else {
+    uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + o);
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) out[i] = pack_bf16(acc[2 * i], acc[2 * i + 1]);
+  }
+}
+
+cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream) {
+  const int rows = a.batch * a.n_h;
+  if (rows == 0) return cudaSuccess;
+  dim3 grid((rows + 3) / 4), block(128);
+  DecodeArgs args = a;
+  void* kargs[] = {&args, &P};
+  const void* fn = head_dim == 128 ? (const void*)reduce_kernel<128> : (const void*)reduce_kernel<64>;
+  return launch_pdl(fn, grid, block, 0, stream, kargs);
+}
+
+}  // namespace pkv
+
+extern "C" const char* pkv_status_str(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument";
+    case PKV_ERANGE: return "size out of range";
+    case PKV_ECUDA: return "CUDA error";
+    case PKV_ENOSPC: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int pkv_last_cuda_error(void) { return pkv::g_last_cuda_error; }

@@ -1,0 +1,56 @@
+"""The C-ABI library builds here (cross-compiled for sm_103a), loads, and exports every
+entry point include/pkv.h declares.  No compute calls: this machine has no GPU."""
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_175_gb300 as pkv
+from paged_kv_cache_175_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    return _build.build_library()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("pkv_kv_append", "pkv_paged_decode_attn", "pkv_kv_quant_append_int4",
+              "pkv_paged_decode_attn_int4", "pkv_rope_shift_k", "pkv_decode_workspace_bytes",
+              "pkv_status_str", "pkv_last_cuda_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    out = subprocess.run(["nm", "-D", "--defined-only", built], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r" T (pkv_\w+)", out))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+
+
+def test_library_loads_and_binding_matches_header(built):
+    l = pkv.lib()
+    for n in _declared():
+        assert hasattr(l, n)
+        assert n in pkv._SIGS, f"binding lacks {n}"
+    assert l.pkv_status_str(0) == b"ok"
+    assert l.pkv_status_str(-4) == b"workspace too small"
+    assert l.pkv_status_str(7) == b"unknown status"
+
+
+def test_binding_refuses_cpu_tensors(built):
+    import torch
+    k = torch.zeros(1, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(pkv.PkvError):
+        pkv.kv_append(k, k, torch.zeros(1, dtype=torch.int64), torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16),
+                      torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16))

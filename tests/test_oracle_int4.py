@@ -62,6 +62,13 @@ def test_constant_group_and_subnormal_scale():
     assert s16 == 0 and not codes.any()
 
 
+def test_zero_minimum_is_positive_zero():
+    codes, s16, m16 = oracle.quantize_group(np.array([-0.0, 0.0, 3.0], np.float32))
+    assert m16.tobytes() == np.float16(0.0).tobytes()
+    _, _, m = oracle.quantize_groups(np.array([[0.0, -0.0], [-0.0, 1.0]], np.float32))
+    assert m.tobytes() == np.zeros(2, np.float16).tobytes()
+
+
 def test_dequant_error_bound_random():
     rng = np.random.default_rng(3)
     for _ in range(200):
@@ -74,6 +81,20 @@ def test_dequant_error_bound_random():
         bound = 0.5 * s + abs(float(m16) - float(x.min())) + 15 * abs(s - s_true) + 1e-6 * np.abs(x).max()
         assert np.max(np.abs(xh - x)) <= bound
         assert codes.max() <= 15
+
+
+def test_vectorised_quantizer_equals_the_scalar_one():
+    rng = np.random.default_rng(7)
+    x = torch.from_numpy(rng.standard_normal((40, 3, 33)).astype(np.float32) * 3).to(torch.bfloat16) \
+        .float().numpy()
+    x[0, 0] = 1.25                                         # a constant group
+    x[1, 1] = np.arange(33) * 2.0 ** -22                   # a range that rounds to a zero scale
+    codes, s16, m16 = oracle.quantize_groups(x)
+    for i in range(40):
+        for j in range(3):
+            c, s, m = oracle.quantize_group(x[i, j])
+            assert np.array_equal(codes[i, j], c)
+            assert s16[i, j].tobytes() == np.float16(s).tobytes() and m16[i, j].tobytes() == np.float16(m).tobytes()
 
 
 def test_pack_order_explicit_bytes():
