@@ -123,7 +123,8 @@ pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* 
  *   s32 = (hi - lo) / 15 (fp32, nearest);
  *   s16 = fp16(s32), m16 = fp16(lo) (nearest even);
  *   code = clamp(rint_half_even((x - m16) / s16), 0, 15) (fp32 subtract / divide),
- *   code = 0 when s16 == 0; dequantized x^ = code * s16 + m16.
+ *   code = 0 when s16 == 0; dequantized x^ = fp16(code * s16 + m16), the exact value
+ *   rounded once to fp16.
  * Groups: V = the head_dim channels of one (token, kv head); K = one channel of one
  * (block, kv head) over the block's block_size rows.  K rows of a block that is not
  * yet full stay in bf16 in `k_tail`; when a call appends a block's last row, the
@@ -156,7 +157,8 @@ pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, const int64_t*
  * its K rows from k_tail[s] (bf16) and its V rows from the codes.
  * Same arguments and output as pkv_paged_decode_attn, with the INT4 tensors in
  * place of the pools; the batch index is the tail row.  q.k and p.v use fp16
- * tensor-core mma with fp32 accumulation.
+ * tensor-core mma with fp32 accumulation (q converted to fp16 once; p carried as an
+ * fp16 high + low pair).  The dequantized values, q and the tail must lie in fp16 range.
  */
 pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, const void* k_meta,
                                       const uint8_t* v_codes, const void* v_meta,

@@ -142,10 +142,16 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
     const int p0 = piece_of(seg_start, W, P), p1 = piece_of(seg_start + nb - 1, W, P);
     if (p0 == p1) return;
     const long long seg = (long long)s * a.n_kv + g;
+    // Only pieces that hold part of the segment wrote a state.  When W < P some pieces
+    // are empty; the piece after p that holds data starts at line position b_{p+1}.
+    auto next_piece = [&](int p) { return piece_of(W * (p + 1) / P, W, P); };
     float M = -INFINITY;
-    for (int p = p0; p <= p1; ++p) M = fmaxf(M, a.ws_ml[((seg + p) * a.G + hl) * 2]);
+    for (int p = p0;; p = next_piece(p)) {
+      M = fmaxf(M, a.ws_ml[((seg + p) * a.G + hl) * 2]);
+      if (p == p1) break;
+    }
     float L = 0.f;
-    for (int p = p0; p <= p1; ++p) {
+    for (int p = p0;; p = next_piece(p)) {
       const long long part = (seg + p) * a.G + hl;
       const float w = ex2(a.ws_ml[part * 2] - M);
       L += w * a.ws_ml[part * 2 + 1];
@@ -157,6 +163,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
         const float2 v = *reinterpret_cast<const float2*>(src);
         acc[0] += w * v.x; acc[1] += w * v.y;
       }
+      if (p == p1) break;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll

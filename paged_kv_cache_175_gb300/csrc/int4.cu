@@ -198,14 +198,16 @@ __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a
 // B-fragment comes from one 16-byte load of its token row: thread t of a quad owns
 // channels [t*D/4, (t+1)*D/4); k-step ks takes word ks/2 and, inside it, channel pairs
 // (0,1),(2,3) or (4,5),(6,7).  The A-fragment (q, converted to fp16 once per segment
-// part) uses the same channel order.  Dequantization x^ = code * s + m runs on half2
-// pairs: the code pair is unpacked into 1024 + code by a mask-and-or, 1024 is
-// subtracted (exact), then one fused multiply-add with the channel pair's (s, m).
+// part) uses the same channel order.  Dequantization x^ = fp16(code * s + m) runs on
+// half2 pairs: the code pair is unpacked into 1024 + code by a mask-and-or, 1024 is
+// subtracted (exact), then one fused multiply-add with the channel pair's (s, m) rounds
+// the exact value once, as the format defines it.
 //
-// P V uses fp16 mma with P rounded once to fp16.  Thread u of a group of four owns
-// output channels [u*D/8, (u+1)*D/8) as B-fragment columns; a byte of a V code word
-// pairs the same nibble of two token rows (byte permute), giving a half2 of two tokens
-// of one channel, scaled by the two tokens' (s, m).
+// P V uses fp16 mma with P carried as an fp16 high part plus an fp16 low part (two mma
+// per tile).  Thread u of a group of four owns output channels [u*D/8, (u+1)*D/8) as
+// B-fragment columns; a byte of a V code word pairs the same nibble of two token rows
+// (byte permute), giving a half2 of two tokens of one channel, scaled by the two
+// tokens' (s, m).
 template <int D, int BS>
 struct Int4Tile {
   static constexpr int KC = 0;
@@ -480,10 +482,14 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
       const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + T::VM);
 #pragma unroll
       for (int kt = 0; kt < BS / 16; ++kt) {
-        uint32_t pa[4];
+        uint32_t pa[4], pl[4];                                    // P = high + low, both fp16
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          pa[i] = pack_f16(sc[2 * kt + (i >> 1)][(i & 1) * 2], sc[2 * kt + (i >> 1)][(i & 1) * 2 + 1]);
+        for (int i = 0; i < 4; ++i) {
+          const float x = sc[2 * kt + (i >> 1)][(i & 1) * 2], y = sc[2 * kt + (i >> 1)][(i & 1) * 2 + 1];
+          pa[i] = pack_f16(x, y);
+          const __half2 h = *reinterpret_cast<const __half2*>(&pa[i]);
+          pl[i] = pack_f16(x - __low2float(h), y - __high2float(h));
+        }
         const int t0 = kt * 16 + 2 * tig;                        // b0: tokens t0, t0+1; b1: t0+8, t0+9
         const uint32_t sA = prmt(vm[t0], vm[t0 + 1], 0x5410), mA = prmt(vm[t0], vm[t0 + 1], 0x7632);
         const uint32_t sB = prmt(vm[t0 + 8], vm[t0 + 9], 0x5410), mB = prmt(vm[t0 + 8], vm[t0 + 9], 0x7632);
@@ -512,6 +518,7 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
                 b1 = b1 & ((t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u));
               }
               mma_f16(o[8 * w + 2 * k + e], pa, b0, b1);
+              mma_f16(o[8 * w + 2 * k + e], pl, b0, b1);
             }
           }
         }

@@ -155,8 +155,9 @@ def test_full_size_step_sampled(name):
     k_before, v_before = f64(kp[idx]), f64(vp[idx])            # the cache before this step's append
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     pkv.kv_append(kn, vn, torch.as_tensor(slots, device=DEV), kp, vp, err=err)
-    out = pkv.paged_decode_attn(q, kp, vp, torch.as_tensor(w.block_tables, device=DEV),
-                                torch.as_tensor(w.context_lens, device=DEV), w.scale, err=err)
+    bt, ctx = torch.as_tensor(w.block_tables, device=DEV), torch.as_tensor(w.context_lens, device=DEV)
+    out = pkv.paged_decode_attn(q, kp, vp, bt, ctx, w.scale, err=err)
+    out32 = pkv.paged_decode_attn(q, kp, vp, bt, ctx, w.scale, out_dtype=torch.float32, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     # oracle: its own append on the compact copy, then attention
@@ -165,4 +166,5 @@ def test_full_size_step_sampled(name):
                        for s in seqs], dtype=np.int64)
     k_after, v_after = oracle.kv_append(k_before, v_before, f64(kn[seqs]), f64(vn[seqs]), cslots, w.block_size)
     ref = oracle.paged_decode_attention(f64(q[seqs]), k_after, v_after, cbt, cctx, w.scale, w.block_size)
+    check_attention(out32[seqs], ref, name)
     check_attention(out[seqs], ref, name)
