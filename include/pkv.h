@@ -116,6 +116,31 @@ pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* 
                                  int32_t* err_flag, void* stream);
 
 /*
+ * paged_decode_attn_noalloc — pkv_paged_decode_attn without a caller workspace.
+ * The reference pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory when they decode (an engine that gave all free memory
+ * to its KV pool, a host program that only receives device pointers from another
+ * runtime, code that must not reach an allocator on its hot path).  Its scratch space
+ * is a fixed array of PKV_STATIC_SCRATCH_BYTES inside the library, held on every GPU
+ * that loads the library until the process exits; the call allocates nothing.
+ *   Arguments, layouts, output and device errors: as pkv_paged_decode_attn, minus the
+ *   workspace.  Returns PKV_ERANGE, without launching anything, when this shape needs
+ *   more scratch than the array holds (pkv_decode_workspace_bytes(..., 0) >
+ *   PKV_STATIC_SCRATCH_BYTES).
+ *   The first call with a given device current looks up the array's device address
+ *   for that device; make that call before any stream capture.
+ *   All calls share the array: calls whose GPU work can overlap (other streams, other
+ *   host threads) race on it and must be serialised by the caller.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+pkv_status pkv_paged_decode_attn_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* block_tables, int max_blocks,
+                                         const int32_t* context_lens, float scale, int batch,
+                                         int n_h, int n_kv, int head_dim, int block_size,
+                                         int num_blocks, void* out, int out_dtype,
+                                         int32_t* err_flag, void* stream);
+
+/*
  * kv_quant_append_int4 — quantize-on-append into an INT4 paged cache.
  * "KVQuant: 마지막 4배": K per channel, V per token, s = (max - min) / 15.
  * Exact op sequence (codes are bit-exact against it):

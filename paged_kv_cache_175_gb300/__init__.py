@@ -39,7 +39,10 @@ _SIGS = {
     "pkv_paged_decode_attn_int4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I,
                                         _I, _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
     "pkv_rope_shift_k": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_double, _P, _P]),
+    "pkv_paged_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
+                                           _P, _I, _P, _P]),
 }
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class PkvError(RuntimeError):
@@ -130,6 +133,21 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, context_lens, scale, out=
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
         float(scale), B, n_h, n_kv, d, bs, num_blocks, _ptr(out), od, _ptr(workspace), workspace.numel(),
         _ptr(err), _stream(stream)))
+    return out
+
+
+def paged_decode_attn_noalloc(q, k_pool, v_pool, block_tables, context_lens, scale, out=None,
+                              out_dtype=torch.bfloat16, err=None, stream=None):
+    """paged_decode_attn with the library's fixed internal scratch instead of a workspace
+    (for callers that cannot allocate device memory; concurrent calls must not overlap)."""
+    _cuda(q, k_pool, v_pool, block_tables, context_lens, out, err)
+    assert q.dtype == k_pool.dtype == v_pool.dtype == torch.bfloat16
+    B, n_h, d = q.shape
+    num_blocks, n_kv, bs, _ = k_pool.shape
+    out, od = _out(q, out, out_dtype)
+    _check("paged_decode_attn_noalloc", lib().pkv_paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        float(scale), B, n_h, n_kv, d, bs, num_blocks, _ptr(out), od, _ptr(err), _stream(stream)))
     return out
 
 

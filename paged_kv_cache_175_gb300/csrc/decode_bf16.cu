@@ -464,3 +464,65 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   }
   return PKV_OK;
 }
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant of pkv_paged_decode_attn.
+//
+// Some callers cannot allocate device memory at decode time: a serving engine that has
+// handed all free device memory to its KV pool up front, a host program that only
+// receives device pointers from another runtime which owns the allocator, or code that
+// must not call into any allocator on its hot path.  For them the scratch space of the
+// decode step lives in a fixed array compiled into this library instead of a
+// caller-provided workspace.  The array is PKV_STATIC_SCRATCH_BYTES large and every GPU
+// that loads the library holds it until the process exits.
+//
+// The device address of the array is looked up once per device, on the first call made
+// with that device current (host code can only name the array's host-side stand-in);
+// make that first call before any stream capture.  Every call shares the one array, so
+// calls whose work overlaps on the GPU (different streams, or different host threads)
+// race on it and must be serialised by the caller.  Nothing in the array needs to start
+// at zero: each call's plan kernel rewrites its prefix sums, and the merge only reads
+// partial states the same call wrote.
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+static void* static_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    record_cuda_error(e);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+extern "C" pkv_status pkv_paged_decode_attn_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                                    const int32_t* block_tables, int max_blocks,
+                                                    const int32_t* context_lens, float scale, int batch, int n_h,
+                                                    int n_kv, int head_dim, int block_size, int num_blocks,
+                                                    void* out, int out_dtype, int32_t* err_flag, void* stream) {
+  if (batch < 0 || !valid_shape(n_h, n_kv, head_dim, block_size)) return PKV_EINVAL;
+  if (batch == 0) return PKV_OK;
+  const size_t need = pkv_decode_workspace_bytes(batch, n_h, n_kv, head_dim, block_size, 0);
+  if (need == 0) {
+    record_cuda_error(cudaGetLastError());
+    return PKV_ECUDA;
+  }
+  if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERANGE;
+  void* ws = static_scratch_address();
+  if (!ws) return PKV_ECUDA;
+  return pkv_paged_decode_attn(q, k_pool, v_pool, block_tables, max_blocks, context_lens, scale, batch, n_h, n_kv,
+                               head_dim, block_size, num_blocks, out, out_dtype, ws, PKV_STATIC_SCRATCH_BYTES,
+                               err_flag, stream);
+}
