@@ -167,11 +167,12 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        rec = json.load(open(p))[f"{kernel}:{workload}"]
+        rec = json.load(open(p))[workload]
     except (OSError, KeyError, ValueError):
         return None
     return rec["bytes_per_launch"] if rec.get("source_hash") == source_hash() else None
@@ -211,14 +212,18 @@ class Bf16Step:
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.launches_per_step = 4          # append, plan, attention, split-reduce
+        self.inputs = {"q": self.q, "kn": self.kn, "vn": self.vn, "slots": self.slots, "bt": self.bt,
+                       "ctx": self.ctx}
 
-    def attention(self):
-        self.pkv.paged_decode_attn(self.q, self.k_pool, self.v_pool, self.bt, self.ctx, self.w.scale,
+    def attention(self, x=None):
+        x = x or self.inputs
+        self.pkv.paged_decode_attn(x["q"], self.k_pool, self.v_pool, x["bt"], x["ctx"], self.w.scale,
                                    out=self.out, workspace=self.ws, err=self.err)
 
-    def step(self):
-        self.pkv.kv_append(self.kn, self.vn, self.slots, self.k_pool, self.v_pool, err=self.err)
-        self.attention()
+    def step(self, x=None):
+        x = x or self.inputs
+        self.pkv.kv_append(x["kn"], x["vn"], x["slots"], self.k_pool, self.v_pool, err=self.err)
+        self.attention(x)
 
     def bytes(self):
         return attention_bytes(self.w) + append_bytes(self.w), attention_bytes(self.w)
@@ -242,6 +247,7 @@ class Int4Step:
                                  torch.as_tensor(np.concatenate(tl), device=dev), self.cache)
         torch.cuda.synchronize()
         del ks, vs
+        torch.cuda.empty_cache()
         self.kn, self.vn = torch.stack(newk).contiguous(), torch.stack(newv).contiguous()
         self.slots = torch.as_tensor(workloads.decode_slots(w), device=dev)
         self.tails = torch.arange(w.batch, dtype=torch.int32, device=dev)
@@ -253,14 +259,18 @@ class Int4Step:
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.launches_per_step = 5          # quantize, tail update, plan, attention, split-reduce
+        self.inputs = {"q": self.q, "kn": self.kn, "vn": self.vn, "slots": self.slots, "tails": self.tails,
+                       "bt": self.bt, "ctx": self.ctx}
 
-    def attention(self):
-        self.pkv.paged_decode_attn_int4(self.q, self.cache, self.bt, self.ctx, self.w.scale, out=self.out,
+    def attention(self, x=None):
+        x = x or self.inputs
+        self.pkv.paged_decode_attn_int4(x["q"], self.cache, x["bt"], x["ctx"], self.w.scale, out=self.out,
                                         workspace=self.ws, err=self.err)
 
-    def step(self):
-        self.pkv.kv_quant_append_int4(self.kn, self.vn, self.slots, self.tails, self.cache, err=self.err)
-        self.attention()
+    def step(self, x=None):
+        x = x or self.inputs
+        self.pkv.kv_quant_append_int4(x["kn"], x["vn"], x["slots"], x["tails"], self.cache, err=self.err)
+        self.attention(x)
 
     def bytes(self):
         return attention_bytes(self.w, True) + append_bytes(self.w, True), attention_bytes(self.w, True)
@@ -276,9 +286,12 @@ class RopeStep:
         self.deltas = torch.as_tensor(w.extra["rope_deltas"], device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.launches_per_step = 1
+        self.out = None
+        self.inputs = {"ids": self.ids, "deltas": self.deltas}
 
-    def step(self):
-        self.pkv.rope_shift_k(self.k_pool, self.ids, self.deltas, err=self.err)
+    def step(self, x=None):
+        x = x or self.inputs
+        self.pkv.rope_shift_k(self.k_pool, x["ids"], x["deltas"], err=self.err)
 
     attention = step
 
@@ -458,21 +471,19 @@ def main():
 
     # ---- end to end through the public API: pinned host inputs in, output back out ----
     w = main_step.w
-    h = {"q": main_step.q.cpu().pin_memory(), "kn": main_step.kn.cpu().pin_memory(),
-         "vn": main_step.vn.cpu().pin_memory(), "slots": main_step.slots.cpu().pin_memory(),
-         "bt": main_step.bt.cpu().pin_memory(), "ctx": main_step.ctx.cpu().pin_memory()}
+    h = {k: v.cpu().pin_memory() for k, v in main_step.inputs.items()}
     d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
-    out_h = torch.empty(main_step.q.shape, dtype=torch.bfloat16).pin_memory()
+    out_h = torch.empty(main_step.out.shape, dtype=main_step.out.dtype).pin_memory() \
+        if main_step.out is not None else None
     h2d = sum(v.numel() * v.element_size() for v in h.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = out_h.numel() * out_h.element_size() if out_h is not None else 0
 
     def e2e_step():
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
-        pkv.kv_append(d["kn"], d["vn"], d["slots"], main_step.k_pool, main_step.v_pool, err=main_step.err)
-        pkv.paged_decode_attn(d["q"], main_step.k_pool, main_step.v_pool, d["bt"], d["ctx"], w.scale,
-                              out=main_step.out, workspace=main_step.ws, err=main_step.err)
-        out_h.copy_(main_step.out, non_blocking=True)
+        main_step.step(d)
+        if out_h is not None:
+            out_h.copy_(main_step.out, non_blocking=True)
 
     ems = time_steps(e2e_step, K, min(W, 3), flush, stream)
     e2e_total = reduce_max(sum(ems), world)
@@ -484,19 +495,24 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {w.n_h} q / {w.n_kv} kv heads, head_dim {w.head_dim}, block "
                                f"{w.block_size}, batch {w.batch}, ctx mean {float(np.mean(w.context_lens)):.0f}",
-                   "step": "kv_append + paged_decode_attn", "parallelism": f"replicas x{world}",
+                   "step": {"Bf16Step": "kv_append + paged_decode_attn",
+                            "Int4Step": "kv_quant_append_int4 + paged_decode_attn_int4",
+                            "RopeStep": "rope_shift_k"}[type(main_step).__name__],
+                   "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (2x L2 write) and inputs larger than L2",
                    "algorithmic_bytes_per_step": step_bytes},
         "seqs_per_s": round(agg["seqs_per_s"], 1),
         "frac_of_hbm_peak": round(agg["gbs"] / world / peak, 4),
         "e2e": {"value": round(e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e["ms_per_step"], 5)},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attn (plan + attention + split-reduce)",
+        "roofline": {"bound": "hbm", "kernel": {"Bf16Step": "paged_decode_attn (plan + attention + split-reduce)",
+                                                "Int4Step": "paged_decode_attn_int4 (plan + attention + split-reduce)",
+                                                "RopeStep": "rope_shift_k"}[type(main_step).__name__],
                      "achieved": round(attn_bytes / (attn_ms / 1e3) / 1e9, 2), "peak": peak,
                      "peak_source": f"{peak_src} (HBM copy, MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(attn_bytes / (attn_ms / 1e3) / 1e9 / peak, 4),
-                     "traffic": recorded_traffic("decode_bf16_kernel", args.workload),
+                     "traffic": recorded_traffic(args.workload),
                      "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 5)},
         "gpu_launches": main_step.launches_per_step * K,
         "clocks": clocks,
@@ -522,7 +538,7 @@ def main():
         line["by_config"] = by
 
     # ---- oracle on the host cores (rank 0, one GPU only) ----
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_budget > 0 and isinstance(main_step, Bf16Step):
         g, s, el, info = time_cpu(cpu_samples(args.workload, 0, 8), args.cpu_budget)
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s", "cores": info["cores"], "kind": "oracle",
                                 "sample": info["sample"], "seqs_per_s": round(s, 3)}

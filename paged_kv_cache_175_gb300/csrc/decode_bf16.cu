@@ -335,8 +335,7 @@ static Bf16Variant make_variant() {
   Bf16Variant v;
   v.fn = (const void*)decode_bf16_kernel<D, BS, MT>;
   v.stage_bytes = Bf16Tile<D, BS>::STAGE;
-  int st = (int)(49152 / v.stage_bytes);
-  v.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
+  v.stages = ring_stages(v.stage_bytes, "PKV_STAGES_BF16");
   v.smem = bf16_smem_bytes<D, BS>(v.stages);
   v.warps = MT;
   v.P = 0;

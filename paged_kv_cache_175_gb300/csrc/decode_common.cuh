@@ -105,6 +105,10 @@ cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t
 cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void** args);
 int device_sm_count();
+// Stages of the shared-memory ring for a stage of `stage_bytes`: about 24 KB of ring per
+// CTA, at least 2 and at most 8; the environment variable `env` (an integer 2..16)
+// overrides it for tuning.
+int ring_stages(size_t stage_bytes, const char* env);
 int mt_for_group(int G);           // consumer warps (16 heads each) per CTA
 int bf16_pieces(int D, int BS, int G);
 int int4_pieces(int D, int BS, int G);

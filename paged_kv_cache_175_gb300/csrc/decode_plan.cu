@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "decode_common.cuh"
@@ -49,6 +50,15 @@ int encode_tensor_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64
                       elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
+int ring_stages(size_t stage_bytes, const char* env) {
+  if (const char* e = getenv(env)) {
+    const int v = atoi(e);
+    if (v >= 2 && v <= 16) return v;
+  }
+  const int st = (int)(24576 / stage_bytes);
+  return st < 2 ? 2 : (st > 8 ? 8 : st);
 }
 
 cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
@@ -126,22 +136,32 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int
 // attention kernel itself; empty sequences get a zero row here.
 template <int D>
 __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) {
-  grid_dep_wait();
+  // The plan kernel finished before the attention kernel started, so cum is readable
+  // before the grid-dependency wait: the index work overlaps the attention kernel's tail.
   constexpr int V = D / 32;                                   // channels per lane
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row >= a.batch * a.n_h) return;
-  const int s = row / a.n_h, h = row % a.n_h, g = h / a.G, hl = h % a.G;
-  const int c0 = a.cum[s], nb = a.cum[s + 1] - c0;
+  const bool live = row < a.batch * a.n_h;
+  int s = 0, h = 0, g = 0, hl = 0, nb = 0, p0 = 0, p1 = 0;
+  long long W = 0, seg = 0;
+  if (live) {
+    s = row / a.n_h; h = row % a.n_h; g = h / a.G; hl = h % a.G;
+    const int c0 = a.cum[s];
+    nb = a.cum[s + 1] - c0;
+    W = (long long)a.n_kv * a.cum[a.batch];
+    if (nb > 0) {
+      const long long seg_start = (long long)a.n_kv * c0 + (long long)g * nb;
+      p0 = piece_of(seg_start, W, P);
+      p1 = piece_of(seg_start + nb - 1, W, P);
+    }
+    seg = (long long)s * a.n_kv + g;
+  }
+  grid_dep_wait();
+  if (!live || (nb > 0 && p0 == p1)) return;                 // finished by the attention kernel
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
   if (nb > 0) {
-    const long long W = (long long)a.n_kv * a.cum[a.batch];
-    const long long seg_start = (long long)a.n_kv * c0 + (long long)g * nb;
-    const int p0 = piece_of(seg_start, W, P), p1 = piece_of(seg_start + nb - 1, W, P);
-    if (p0 == p1) return;
-    const long long seg = (long long)s * a.n_kv + g;
     // Only pieces that hold part of the segment wrote a state.  When W < P some pieces
     // are empty; the piece after p that holds data starts at line position b_{p+1}.
     auto next_piece = [&](int p) { return piece_of(W * (p + 1) / P, W, P); };

@@ -609,8 +609,7 @@ static Int4Variant make_int4_variant() {
   Int4Variant v;
   v.fn = (const void*)decode_int4_kernel<D, BS, MT>;
   const int stage = Int4Tile<D, BS>::STAGE;
-  int st = 49152 / stage;
-  v.stages = st < 2 ? 2 : (st > 8 ? 8 : st);
+  v.stages = ring_stages(stage, "PKV_STAGES_INT4");
   v.smem = int4_smem_bytes<D, BS>(v.stages);
   v.warps = MT;
   v.P = 0;

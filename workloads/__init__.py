@@ -97,7 +97,21 @@ def _tables(ctx: np.ndarray, bs: int, rng: np.random.Generator, pool_factor: flo
 
 
 def make(name: str, seed: int = 0) -> Workload:
-    """Shapes, context lengths and block tables of a named workload (host only)."""
+    """Shapes, context lengths and block tables of a named workload (host only).
+
+    A suffix ``_b<N>`` keeps the first N context lengths of the named workload with a
+    pool sized for them (a smaller case of the same shape, e.g. for profiler captures).
+    """
+    base, _, nb = name.rpartition("_b")
+    if base and nb.isdigit() and base in NAMES:
+        w = make(base, seed)
+        n = int(nb)
+        ctx = w.context_lens[:n].copy()
+        bt, nbk = _tables(ctx, w.block_size, np.random.default_rng(seed + 1), 1.2,
+                          shared=w.shared_prefix_blocks, n_sharers=min(w.n_sharers, n))
+        return Workload(name, n, w.n_h, w.n_kv, w.head_dim, w.block_size, ctx, bt, nbk, w.scale,
+                        shared_prefix_blocks=w.shared_prefix_blocks if min(w.n_sharers, n) else 0,
+                        n_sharers=min(w.n_sharers, n), outlier_channels=w.outlier_channels, extra=w.extra)
     rng = np.random.default_rng(seed)
     if name == "tiny":
         ctx = np.array([17, 64, 100, 255], dtype=np.int32)
