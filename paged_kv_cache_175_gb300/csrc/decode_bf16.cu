@@ -38,14 +38,15 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t b, int t, int ntok) {
   return b & ((t < ntok ? 0x0000ffffu : 0u) | (t + 1 < ntok ? 0xffff0000u : 0u));
 }
 
-template <int D, int BS, int MT>
+template <int D, int BS, int NH, int MT>
 __global__ void __launch_bounds__(MT * 32)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const DecodeArgs a) {
   using T = Bf16Tile<D, BS>;
-  constexpr int NT = BS / 8;        // score n-tiles of 8 tokens
-  constexpr int KS = D / 16;        // k-steps of Q K^T
-  constexpr int DN = D / 8;         // output n-tiles of 8 channels
+  constexpr int TT = BS / 16;       // 16-token tiles per block
+  constexpr int KS = D / 16;        // k-steps of K Q^T
+  constexpr int MD = D / 16;        // 16-channel m-tiles of O^T
+  constexpr int HW = 8 * NH;        // heads per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
@@ -70,7 +71,8 @@ __global__ void __launch_bounds__(MT * 32)
   grid_dep_launch();
 
   const long long W = (long long)a.n_kv * a.cum[a.batch];
-  const int P = gridDim.x, p = blockIdx.x;
+  const int P = effective_pieces(W, gridDim.x), p = blockIdx.x;
+  if (p >= P) return;
   const long long pstart = W * p / P, pend = W * (p + 1) / P;
   const int len = (int)(pend - pstart);
   if (len <= 0) return;
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(MT * 32)
   Cursor cur;
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
-  if (warp == 0) cursor_init(cur, pstart, a);
+  if (warp == 0) cursor_from_table(cur, p, pstart, a);
 
   auto issue = [&](int j) {
     if (cur.s != w_seq || cur.blk < w_base || cur.blk >= w_base + 32) {
@@ -131,13 +133,15 @@ __global__ void __launch_bounds__(MT * 32)
     if (j + 1 < len) cursor_next(cur, a);
   };
 
-  // ---------------- consumer state (every warp: 16 heads) ----------------
-  uint32_t qa[KS][4];
-  float o[DN][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int r0 = lane >> 2;                      // rows r0 and r0 + 8 of the m-tile
-  const int hl0 = warp * 16 + r0, hl1 = hl0 + 8; // local head index inside the group
-  const bool v0 = hl0 < a.G, v1 = hl1 < a.G;
+  // ---------------- consumer state (warp w: local heads [w*HW, (w+1)*HW)) ----------------
+  // Token-major tiles: S^T[token][head] = K Q^T with the block's tokens on the mma M side
+  // and this warp's heads on N (8 per n-tile), then O^T[channel][head] = V^T P^T with
+  // P^T's fragments made from S^T's by an in-register 8x8 transpose (movmatrix).
+  uint32_t qb[KS][NH][2];
+  float o[MD][NH][4];
+  float m[NH][2], l[NH][2];
+  const int gid = lane >> 2;                    // token row / channel row / head column
+  const int hw0 = warp * HW;                    // first local head of this warp
 
   if (warp == 0) {
     const int pre = len < S ? len : S;
@@ -155,155 +159,199 @@ __global__ void __launch_bounds__(MT * 32)
     consumed = j + 1;
     const int4 mt = meta[slot];
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = mt.w >> 8;
+    const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;   // first q head of the group
 
     if (flags & F_FIRST) {
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q) + ((size_t)s * a.n_h + (size_t)g * a.G + hl0) * (D / 2);
-      const uint32_t* q1 = q0 + 8 * (D / 2);
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qa[ks][0] = v0 ? __ldg(q0 + ks * 8 + tig) : 0u;
-        qa[ks][1] = v1 ? __ldg(q1 + ks * 8 + tig) : 0u;
-        qa[ks][2] = v0 ? __ldg(q0 + ks * 8 + 4 + tig) : 0u;
-        qa[ks][3] = v1 ? __ldg(q1 + ks * 8 + 4 + tig) : 0u;
+      for (int nh = 0; nh < NH; ++nh) {
+        const int hl = hw0 + nh * 8 + gid;                       // B-fragment column n = gid
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q) + (qrow0 + hl) * (D / 2);
+        const bool ok = hl < a.G;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qb[ks][nh][0] = ok ? __ldg(qp + ks * 8 + tig) : 0u;
+          qb[ks][nh][1] = ok ? __ldg(qp + ks * 8 + 4 + tig) : 0u;
+        }
+        m[nh][0] = m[nh][1] = -INFINITY;
+        l[nh][0] = l[nh][1] = 0.f;
+#pragma unroll
+        for (int md = 0; md < MD; ++md) o[md][nh][0] = o[md][nh][1] = o[md][nh][2] = o[md][nh][3] = 0.f;
       }
-#pragma unroll
-      for (int n = 0; n < DN; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
     }
 
     if (flags & F_VALID) {
       const uint32_t kb = smem_u32(smem + (size_t)slot * T::STAGE), vb = kb + T::TILE;
-      float sc[NT][4];
+      // ---- S^T = K Q^T: per 16-token tile and head n-tile, two accumulators (even / odd
+      // k-steps) so the dependent mma chains are half as long ----
+      float sc[TT][NH][4];
+      {
+        float sx[TT][NH][4];
 #pragma unroll
-      for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-      // S = Q K^T
+        for (int t = 0; t < TT; ++t)
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
+          for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          const int tok = np * 16 + ((lane >> 4) << 3) + (lane & 7);
-          const int ch = 2 * ks + ((lane >> 3) & 1);
-          const uint32_t addr = kb + (ch >> 3) * T::BOX_BYTES + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(b0, b1, b2, b3, addr);
-          mma_bf16(sc[2 * np], qa[ks], b0, b1);
-          mma_bf16(sc[2 * np + 1], qa[ks], b2, b3);
+            for (int i = 0; i < 4; ++i) sc[t][nh][i] = sx[t][nh][i] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            const int mi = lane >> 3;
+            const int tok = t * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int ch = 2 * ks + (mi >> 1);
+            const uint32_t addr = kb + (ch >> 3) * T::BOX_BYTES + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
+            uint32_t ka[4];
+            ldsm_x4(ka[0], ka[1], ka[2], ka[3], addr);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+              if (ks & 1) mma_bf16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+              else mma_bf16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+            }
+          }
         }
-      }
-      // online softmax (base 2)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[t][nh][i] += sx[t][nh][i];
+      }
+      // ---- online softmax over tokens (rows), per head (column), base 2 ----
+      float al[NH][2];
+      bool rescale = false;
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int tok = n * 8 + 2 * tig + e;
-          float x0 = sc[n][e] * a.scale_log2, x1 = sc[n][2 + e] * a.scale_log2;
-          if (tok >= ntok) x0 = x1 = -INFINITY;
-          sc[n][e] = x0;
-          sc[n][2 + e] = x1;
-          mx0 = fmaxf(mx0, x0);
-          mx1 = fmaxf(mx1, x1);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int tok = t * 16 + gid + 8 * r;
+              float x = sc[t][nh][2 * r + e] * a.scale_log2;
+              if (tok >= ntok) x = -INFINITY;
+              sc[t][nh][2 * r + e] = x;
+              mx = fmaxf(mx, x);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+          const float mn = fmaxf(m[nh][e], mx);
+          al[nh][e] = ex2(m[nh][e] - mn);
+          rescale |= al[nh][e] != 1.f;
+          m[nh][e] = mn;
+          float rs = 0.f;
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float p = ex2(sc[t][nh][2 * r + e] - mn);
+              sc[t][nh][2 * r + e] = p;
+              rs += p;
+            }
+          l[nh][e] = l[nh][e] * al[nh][e] + rs;
         }
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float rs0 = 0.f, rs1 = 0.f;
+      if (__any_sync(FULL_MASK, rescale)) {
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
+        for (int md = 0; md < MD; ++md)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          sc[n][e] = ex2(sc[n][e] - mn0);
-          sc[n][2 + e] = ex2(sc[n][2 + e] - mn1);
-          rs0 += sc[n][e];
-          rs1 += sc[n][2 + e];
-        }
+          for (int nh = 0; nh < NH; ++nh) {
+            o[md][nh][0] *= al[nh][0]; o[md][nh][1] *= al[nh][1];
+            o[md][nh][2] *= al[nh][0]; o[md][nh][3] *= al[nh][1];
+          }
       }
-      l0 = l0 * al0 + rs0;
-      l1 = l1 * al1 + rs1;
-      if (__any_sync(FULL_MASK, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-        for (int n = 0; n < DN; ++n) {
-          o[n][0] *= al0; o[n][1] *= al0; o[n][2] *= al1; o[n][3] *= al1;
-        }
-      }
-      // O += P V, P as bf16 high + low
+      // ---- O^T += V^T P^T, P as bf16 high + low ----
       const bool partial = ntok < BS;
 #pragma unroll
-      for (int kt = 0; kt < BS / 16; ++kt) {
-        uint32_t ah[4], al[4];
+      for (int t = 0; t < TT; ++t) {
+        // B fragments of P^T (k = token, n = head): the S^T rows of tokens 0-7 / 8-15 of
+        // the tile, packed per head pair and transposed
+        uint32_t bh[NH][2], bl[NH][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x = sc[2 * kt + (i >> 1)][(i & 1) * 2], y = sc[2 * kt + (i >> 1)][(i & 1) * 2 + 1];
-          ah[i] = pack_bf16(x, y);
-          al[i] = pack_bf16(x - bf16_lo(ah[i]), y - bf16_hi(ah[i]));
-        }
-        const int t0 = kt * 16 + 2 * tig;
+        for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int nb = 0; nb < D / 16; ++nb) {
-          const int tok = kt * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-          const int ch = 2 * nb + (lane >> 4);
-          const uint32_t addr = vb + (ch >> 3) * T::BOX_BYTES + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(b0, b1, b2, b3, addr);
-          if (partial) {
-            b0 = mask_pair(b0, t0, ntok);
-            b2 = mask_pair(b2, t0, ntok);
-            b1 = mask_pair(b1, t0 + 8, ntok);
-            b3 = mask_pair(b3, t0 + 8, ntok);
+          for (int r = 0; r < 2; ++r) {
+            const float x = sc[t][nh][2 * r], y = sc[t][nh][2 * r + 1];
+            const uint32_t hi = pack_bf16(x, y);
+            const uint32_t lo = pack_bf16(x - bf16_lo(hi), y - bf16_hi(hi));
+            bh[nh][r] = movmatrix_t(hi);
+            bl[nh][r] = movmatrix_t(lo);
           }
-          mma_bf16(o[2 * nb], ah, b0, b1);
-          mma_bf16(o[2 * nb], al, b0, b1);
-          mma_bf16(o[2 * nb + 1], ah, b2, b3);
-          mma_bf16(o[2 * nb + 1], al, b2, b3);
+        const int t0 = t * 16 + 2 * tig;                   // a0/a1: tokens t0, t0+1; a2/a3: +8
+#pragma unroll
+        for (int md = 0; md < MD; ++md) {
+          const int mi = lane >> 3;
+          const int tok = t * 16 + ((mi >> 1) << 3) + (lane & 7);
+          const int ch = 2 * md + (mi & 1);
+          const uint32_t addr = vb + (ch >> 3) * T::BOX_BYTES + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
+          uint32_t va[4];
+          ldsm_x4_t(va[0], va[1], va[2], va[3], addr);
+          if (partial) {
+            va[0] = mask_pair(va[0], t0, ntok);
+            va[1] = mask_pair(va[1], t0, ntok);
+            va[2] = mask_pair(va[2], t0 + 8, ntok);
+            va[3] = mask_pair(va[3], t0 + 8, ntok);
+          }
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) {
+            mma_bf16(o[md][nh], va, bh[nh][0], bh[nh][1]);
+            mma_bf16(o[md][nh], va, bl[nh][0], bl[nh][1]);
+          }
         }
       }
     }
 
     if (flags & F_LAST) {
-      float L0 = l0 + __shfl_xor_sync(FULL_MASK, l0, 1);
-      L0 += __shfl_xor_sync(FULL_MASK, L0, 2);
-      float L1 = l1 + __shfl_xor_sync(FULL_MASK, l1, 1);
-      L1 += __shfl_xor_sync(FULL_MASK, L1, 2);
-      if (flags & F_WHOLE) {
-        const float i0 = L0 > 0.f ? 1.f / L0 : 0.f, i1 = L1 > 0.f ? 1.f / L1 : 0.f;
-        const size_t row0 = (size_t)s * a.n_h + (size_t)g * a.G + hl0;
-        if (a.out_f32) {
-          float* out0 = reinterpret_cast<float*>(a.out) + row0 * D;
-          float* out1 = out0 + 8 * D;
+      float L[NH][2];
 #pragma unroll
-          for (int n = 0; n < DN; ++n) {
-            if (v0) *reinterpret_cast<float2*>(out0 + n * 8 + 2 * tig) = make_float2(o[n][0] * i0, o[n][1] * i0);
-            if (v1) *reinterpret_cast<float2*>(out1 + n * 8 + 2 * tig) = make_float2(o[n][2] * i1, o[n][3] * i1);
+      for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float x = l[nh][e];
+          x += __shfl_xor_sync(FULL_MASK, x, 4);
+          x += __shfl_xor_sync(FULL_MASK, x, 8);
+          x += __shfl_xor_sync(FULL_MASK, x, 16);
+          L[nh][e] = x;
+        }
+      const bool whole = flags & F_WHOLE;
+      const long long part = (long long)s * a.n_kv + g + p;
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hl = hw0 + nh * 8 + 2 * tig + e;           // this thread's head columns
+          if (hl >= a.G) continue;
+          const float inv = whole ? (L[nh][e] > 0.f ? 1.f / L[nh][e] : 0.f) : 1.f;
+          if (whole) {
+            const size_t base = (qrow0 + hl) * D;
+            if (a.out_f32) {
+              float* out = reinterpret_cast<float*>(a.out) + base;
+#pragma unroll
+              for (int md = 0; md < MD; ++md) {
+                out[md * 16 + gid] = o[md][nh][e] * inv;
+                out[md * 16 + gid + 8] = o[md][nh][2 + e] * inv;
+              }
+            } else {
+              __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + base;
+#pragma unroll
+              for (int md = 0; md < MD; ++md) {
+                out[md * 16 + gid] = __float2bfloat16_rn(o[md][nh][e] * inv);
+                out[md * 16 + gid + 8] = __float2bfloat16_rn(o[md][nh][2 + e] * inv);
+              }
+            }
+          } else {
+            float* wo = a.ws_o + ((size_t)part * a.G + hl) * D;
+#pragma unroll
+            for (int md = 0; md < MD; ++md) {
+              wo[md * 16 + gid] = o[md][nh][e];
+              wo[md * 16 + gid + 8] = o[md][nh][2 + e];
+            }
+            if (gid == 0)
+              *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl) * 2) = make_float2(m[nh][e], L[nh][e]);
           }
-        } else {
-          uint32_t* out0 = reinterpret_cast<uint32_t*>(a.out) + row0 * (D / 2);
-          uint32_t* out1 = out0 + 8 * (D / 2);
-#pragma unroll
-          for (int n = 0; n < DN; ++n) {
-            if (v0) out0[n * 4 + tig] = pack_bf16(o[n][0] * i0, o[n][1] * i0);
-            if (v1) out1[n * 4 + tig] = pack_bf16(o[n][2] * i1, o[n][3] * i1);
-          }
         }
-      } else {
-        const long long part = (long long)s * a.n_kv + g + p;
-        float* wo = a.ws_o + (size_t)part * a.G * D;
-#pragma unroll
-        for (int n = 0; n < DN; ++n) {
-          if (v0) *reinterpret_cast<float2*>(wo + (size_t)hl0 * D + n * 8 + 2 * tig) = make_float2(o[n][0], o[n][1]);
-          if (v1) *reinterpret_cast<float2*>(wo + (size_t)hl1 * D + n * 8 + 2 * tig) = make_float2(o[n][2], o[n][3]);
-        }
-        if (tig == 0) {
-          if (v0) *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl0) * 2) = make_float2(m0, L0);
-          if (v1) *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl1) * 2) = make_float2(m1, L1);
-        }
-      }
     }
 
     __syncwarp();
@@ -330,10 +378,10 @@ struct Bf16Variant {
   int P;        // persistent CTAs on this device
 };
 
-template <int D, int BS, int MT>
+template <int D, int BS, int NH, int MT>
 static Bf16Variant make_variant() {
   Bf16Variant v;
-  v.fn = (const void*)decode_bf16_kernel<D, BS, MT>;
+  v.fn = (const void*)decode_bf16_kernel<D, BS, NH, MT>;
   v.stage_bytes = Bf16Tile<D, BS>::STAGE;
   v.stages = ring_stages(v.stage_bytes, "PKV_STAGES_BF16");
   v.smem = bf16_smem_bytes<D, BS>(v.stages);
@@ -344,23 +392,28 @@ static Bf16Variant make_variant() {
 
 int mt_for_group(int G) { return G <= 16 ? 1 : (G <= 32 ? 2 : 4); }
 
-static Bf16Variant* lookup_bf16(int D, int BS, int MT) {
+// Head tiling of a group: G <= 8 -> one warp with one 8-head n-tile; otherwise warps of
+// two 8-head n-tiles (16 heads each), ceil(G / 16) of them rounded up to 1, 2 or 4.
+// Variant index: 0 (NH 1, MT 1), 1 (2, 1), 2 (2, 2), 3 (2, 4).
+static int bf16_tiling(int G) { return G <= 8 ? 0 : (G <= 16 ? 1 : (G <= 32 ? 2 : 3)); }
+
+static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   // One table per process; the library drives one device per process.
   static std::mutex mu;
-  static Bf16Variant table[2][3][3];
-  static bool ready[2][3][3] = {};
-  const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2), mi = MT == 1 ? 0 : (MT == 2 ? 1 : 2);
+  static Bf16Variant table[2][3][4];
+  static bool ready[2][3][4] = {};
+  const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2), ti = tiling;
   std::lock_guard<std::mutex> lock(mu);
-  Bf16Variant& v = table[di][bi][mi];
-  if (!ready[di][bi][mi]) {
-#define PKV_V(d, b, m) \
-  if (D == d && BS == b && MT == m) v = make_variant<d, b, m>();
-    PKV_V(64, 16, 1) PKV_V(64, 16, 2) PKV_V(64, 16, 4)
-    PKV_V(64, 32, 1) PKV_V(64, 32, 2) PKV_V(64, 32, 4)
-    PKV_V(64, 64, 1) PKV_V(64, 64, 2) PKV_V(64, 64, 4)
-    PKV_V(128, 16, 1) PKV_V(128, 16, 2) PKV_V(128, 16, 4)
-    PKV_V(128, 32, 1) PKV_V(128, 32, 2) PKV_V(128, 32, 4)
-    PKV_V(128, 64, 1) PKV_V(128, 64, 2) PKV_V(128, 64, 4)
+  Bf16Variant& v = table[di][bi][ti];
+  if (!ready[di][bi][ti]) {
+#define PKV_V(d, b)                                               \
+  if (D == d && BS == b) {                                        \
+    if (ti == 0) v = make_variant<d, b, 1, 1>();                  \
+    else if (ti == 1) v = make_variant<d, b, 2, 1>();             \
+    else if (ti == 2) v = make_variant<d, b, 2, 2>();             \
+    else v = make_variant<d, b, 2, 4>();                          \
+  }
+    PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
     if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v.smem) != cudaSuccess)
       return nullptr;
@@ -368,13 +421,13 @@ static Bf16Variant* lookup_bf16(int D, int BS, int MT) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.warps * 32, v.smem) != cudaSuccess || occ < 1)
       return nullptr;
     v.P = device_sm_count() * occ;
-    ready[di][bi][mi] = true;
+    ready[di][bi][ti] = true;
   }
   return &v;
 }
 
 int bf16_pieces(int D, int BS, int G) {
-  Bf16Variant* v = lookup_bf16(D, BS, mt_for_group(G));
+  Bf16Variant* v = lookup_bf16(D, BS, bf16_tiling(G));
   return v ? v->P : 0;
 }
 
@@ -413,8 +466,8 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   if (!al16(q) || !al16(k_pool) || !al16(v_pool) || !al16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PKV_EINVAL;
   if ((long long)max_blocks * block_size > 0x7fffffffLL) return PKV_ERANGE;
-  const int G = n_h / n_kv, MT = mt_for_group(G);
-  Bf16Variant* v = lookup_bf16(head_dim, block_size, MT);
+  const int G = n_h / n_kv;
+  Bf16Variant* v = lookup_bf16(head_dim, block_size, bf16_tiling(G));
   if (!v) {
     record_cuda_error(cudaGetLastError());
     return PKV_ECUDA;
@@ -437,6 +490,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   a.max_blocks = max_blocks;
   a.cum = reinterpret_cast<int32_t*>(ws + wl.cum);
   a.ctx_eff = reinterpret_cast<int32_t*>(ws + wl.ctx);
+  a.pieces = reinterpret_cast<int4*>(ws + wl.pieces);
   a.batch = batch;
   a.n_h = n_h;
   a.n_kv = n_kv;
@@ -451,7 +505,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   a.stages = v->stages;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_plan(context_lens, batch, max_blocks * block_size, block_size, a, st);
+  cudaError_t e = launch_plan(context_lens, batch, max_blocks * block_size, block_size, a, v->P, st);
   if (e == cudaSuccess) {
     void* kargs[] = {&tmk, &tmv, &a};
     e = launch_pdl(v->fn, dim3(v->P), dim3(v->warps * 32), v->smem, st, kargs);

@@ -24,6 +24,7 @@ struct DecodeArgs {
   int max_blocks;
   const int32_t* cum;            // workspace: [B+1] exclusive prefix of blocks per sequence
   const int32_t* ctx_eff;        // workspace: [B] context lengths after range checks
+  const int4* pieces;            // workspace: [P][2] start cursor of each piece (s, g, blk, nb | ctx)
   int batch, n_h, n_kv, G, num_blocks;
   float scale_log2;              // scale * log2(e): softmax runs in base 2
   void* out;
@@ -41,8 +42,17 @@ struct DecodeArgs {
 };
 
 struct WorkspaceLayout {
-  size_t cum, ctx, ml, o, total;
+  size_t cum, ctx, pieces, ml, o, total;
 };
+
+// Pieces actually used for a line of W positions when P CTAs are launched: at least
+// kMinPiece positions per piece, so a small batch is not cut into one-tile parts whose
+// merge would cost more than streaming them.
+constexpr int kMinPiece = 16;
+__host__ __device__ inline int effective_pieces(long long W, int P) {
+  const long long q = (W + kMinPiece - 1) / kMinPiece;
+  return (int)(q < 1 ? 1 : (q < P ? q : P));
+}
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -51,7 +61,8 @@ __host__ inline WorkspaceLayout workspace_layout(int B, int n_kv, int G, int D, 
   const size_t parts = (size_t)B * n_kv + (size_t)P;
   w.cum = 0;
   w.ctx = align_up(sizeof(int32_t) * (size_t)(B + 1), 16);
-  w.ml = align_up(w.ctx + sizeof(int32_t) * (size_t)B, 256);
+  w.pieces = align_up(w.ctx + sizeof(int32_t) * (size_t)B, 32);
+  w.ml = align_up(w.pieces + 2 * sizeof(int4) * (size_t)P, 256);
   w.o = align_up(w.ml + sizeof(float) * parts * G * 2, 256);
   w.total = align_up(w.o + sizeof(float) * parts * G * D, 256);
   return w;
@@ -68,19 +79,15 @@ struct Cursor {
   long long seg_start;           // line position of block 0 of segment (s, g)
 };
 
-__device__ __forceinline__ void cursor_init(Cursor& c, long long pos, const DecodeArgs& a) {
-  int lo = 0, hi = a.batch - 1;
-  while (lo < hi) {                                  // largest s with n_kv * cum[s] <= pos
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)a.n_kv * a.cum[mid] <= pos) lo = mid; else hi = mid - 1;
-  }
-  c.s = lo;
-  c.nb = a.cum[lo + 1] - a.cum[lo];
-  c.ctx = a.ctx_eff[lo];
-  const long long off = pos - (long long)a.n_kv * a.cum[lo];
-  c.g = (int)(off / c.nb);
-  c.blk = (int)(off % c.nb);
-  c.seg_start = pos - c.blk;
+// Start cursor of piece p, precomputed by the plan kernel (one 32-byte load).
+__device__ __forceinline__ void cursor_from_table(Cursor& c, int p, long long pstart, const DecodeArgs& a) {
+  const int4 e0 = a.pieces[2 * p], e1 = a.pieces[2 * p + 1];
+  c.s = e0.x;
+  c.g = e0.y;
+  c.blk = e0.z;
+  c.nb = e0.w;
+  c.ctx = e1.x;
+  c.seg_start = pstart - c.blk;
 }
 
 // Advance by one position; only called while positions remain, so a non-empty
@@ -100,7 +107,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
 
 // Host launchers (decode_plan.cu).
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,
-                        const DecodeArgs& a, cudaStream_t stream);
+                        const DecodeArgs& a, int P, cudaStream_t stream);
 cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream);
 cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void** args);

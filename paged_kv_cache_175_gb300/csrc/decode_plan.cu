@@ -76,13 +76,21 @@ cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cud
   return cudaLaunchKernelExC(&cfg, func, args);
 }
 
-// ---- plan: range-check context lengths and scan blocks per sequence ---------------------------
+// ---- plan: range-check context lengths, scan blocks per sequence, start cursors ---------------
+// One CTA.  The prefix sums also go to shared memory (up to kPlanSeqs sequences; beyond
+// that the cursor search reads them back from global memory, which this CTA wrote), and
+// every piece's start cursor is computed here so an attention CTA begins with one load.
+constexpr int kPlanSeqs = 8192;
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ ctx, int batch, int max_ctx,
-                                                    int block_size, int32_t* __restrict__ cum,
-                                                    int32_t* __restrict__ ctx_eff, int32_t* err) {
+                                                    int block_size, int n_kv, int P, int32_t* __restrict__ cum,
+                                                    int32_t* __restrict__ ctx_eff, int4* __restrict__ pieces,
+                                                    int32_t* err) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
+  __shared__ int scum[kPlanSeqs + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool in_smem = batch <= kPlanSeqs;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   for (int base = 0; base < batch; base += 1024) {
@@ -116,18 +124,42 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
     __syncthreads();
     const int excl = carry + (warp ? warp_sums[warp - 1] : 0) + x - nb;
-    if (s < batch) cum[s] = excl;
+    if (s < batch) {
+      cum[s] = excl;
+      if (in_smem) scum[s] = excl;
+    }
     __syncthreads();
     if (threadIdx.x == 1023) carry = excl + nb;
     __syncthreads();
   }
-  if (threadIdx.x == 0) cum[batch] = carry;
+  if (threadIdx.x == 0) {
+    cum[batch] = carry;
+    if (in_smem) scum[batch] = carry;
+  }
+  __syncthreads();
+  const int* cu = in_smem ? scum : cum;
+  const long long W = (long long)n_kv * carry;
+  const int Pe = effective_pieces(W, P);
+  for (int p = threadIdx.x; p < Pe; p += blockDim.x) {
+    const long long pstart = W * p / Pe;
+    if (pstart >= W) continue;                                // W == 0: nothing to start
+    int lo = 0, hi = batch - 1;                               // largest s with n_kv * cum[s] <= pstart
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)n_kv * cu[mid] <= pstart) lo = mid; else hi = mid - 1;
+    }
+    const int nb = cu[lo + 1] - cu[lo];
+    const long long off = pstart - (long long)n_kv * cu[lo];
+    pieces[2 * p] = make_int4(lo, (int)(off / nb), (int)(off % nb), nb);
+    pieces[2 * p + 1] = make_int4(ctx_eff[lo], 0, 0, 0);
+  }
 }
 
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,
-                        const DecodeArgs& a, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(context_lens, batch, max_ctx, block_size,
-                                      const_cast<int32_t*>(a.cum), const_cast<int32_t*>(a.ctx_eff), a.err);
+                        const DecodeArgs& a, int P, cudaStream_t stream) {
+  plan_kernel<<<1, 1024, 0, stream>>>(context_lens, batch, max_ctx, block_size, a.n_kv, P,
+                                      const_cast<int32_t*>(a.cum), const_cast<int32_t*>(a.ctx_eff),
+                                      const_cast<int4*>(a.pieces), a.err);
   return cudaGetLastError();
 }
 
@@ -149,6 +181,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
     const int c0 = a.cum[s];
     nb = a.cum[s + 1] - c0;
     W = (long long)a.n_kv * a.cum[a.batch];
+    P = effective_pieces(W, P);
     if (nb > 0) {
       const long long seg_start = (long long)a.n_kv * c0 + (long long)g * nb;
       p0 = piece_of(seg_start, W, P);
@@ -164,26 +197,55 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
   if (nb > 0) {
     // Only pieces that hold part of the segment wrote a state.  When W < P some pieces
     // are empty; the piece after p that holds data starts at line position b_{p+1}.
-    auto next_piece = [&](int p) { return piece_of(W * (p + 1) / P, W, P); };
-    float M = -INFINITY;
-    for (int p = p0;; p = next_piece(p)) {
-      M = fmaxf(M, a.ws_ml[((seg + p) * a.G + hl) * 2]);
-      if (p == p1) break;
-    }
-    float L = 0.f;
-    for (int p = p0;; p = next_piece(p)) {
-      const long long part = (seg + p) * a.G + hl;
-      const float w = ex2(a.ws_ml[part * 2] - M);
-      L += w * a.ws_ml[part * 2 + 1];
-      const float* src = a.ws_o + part * D + lane * V;
-      if constexpr (V == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y;
+    // Parts are merged in chunks of CH with every load of a chunk issued before any is
+    // used (one memory round trip per chunk instead of one per part), online across chunks.
+    constexpr int CH = 8;
+    float M = -INFINITY, L = 0.f;
+    int p = p0;
+    bool more = true;
+    while (more) {
+      float mv[CH], lv[CH], ov[CH][V];
+      bool use[CH];
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        use[i] = more;
+        mv[i] = -INFINITY;
+        lv[i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < V; ++k) ov[i][k] = 0.f;
+        if (more) {
+          const long long part = (seg + p) * a.G + hl;
+          const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + part * 2);
+          mv[i] = ml.x;
+          lv[i] = ml.y;
+          const float* src = a.ws_o + part * D + lane * V;
+          if constexpr (V == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            ov[i][0] = v.x; ov[i][1] = v.y; ov[i][2] = v.z; ov[i][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            ov[i][0] = v.x; ov[i][1] = v.y;
+          }
+          if (p == p1) more = false;
+          else p = piece_of(W * (p + 1) / P, W, P);
+        }
       }
-      if (p == p1) break;
+      float Mc = M;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) Mc = fmaxf(Mc, mv[i]);
+      const float r = ex2(M - Mc);                            // rescale what was merged so far
+      L *= r;
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] *= r;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        if (!use[i]) continue;
+        const float w = ex2(mv[i] - Mc);
+        L += w * lv[i];
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc[k] += w * ov[i][k];
+      }
+      M = Mc;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll

@@ -18,6 +18,10 @@ def bounds(p, W, P):
     return W * p // P, W * (p + 1) // P
 
 
+def effective_pieces(W, P, min_piece=16):
+    return max(1, min(P, -(-W // min_piece)))
+
+
 @pytest.mark.parametrize("W,P", [(10, 4), (20, 608), (58, 608), (75000, 608), (7, 7), (1, 152), (999, 1000)])
 def test_piece_of_matches_brute_force(W, P):
     owner = np.full(W, -1)
@@ -40,6 +44,9 @@ def test_segment_walk_and_part_indices(seed):
     if W == 0:
         return
     P = int(rng.choice([3, 50, 608, W, 2 * W + 1]))
+    if seed % 2:
+        P = effective_pieces(W, P)          # the kernels cap the grid at ceil(W / 16) pieces
+        assert all(bounds(p, W, P)[1] > bounds(p, W, P)[0] for p in range(P))   # no empty piece
     parts = set()
     for s in range(B):
         for g in range(n_kv):
