@@ -70,18 +70,18 @@ __global__ void __launch_bounds__(MT * 32)
   grid_dep_wait();                  // plan kernel's cum / ctx_eff are visible after this
   grid_dep_launch();
 
-  const long long W = (long long)a.n_kv * a.cum[a.batch];
-  const int P = effective_pieces(W, gridDim.x), p = blockIdx.x;
+  Cursor cur;
+  PieceInfo pi;
+  piece_setup(a, blockIdx.x, gridDim.x, warp == 0, cur, pi);
+  const int P = pi.P, p = blockIdx.x;
   if (p >= P) return;
-  const long long pstart = W * p / P, pend = W * (p + 1) / P;
+  const long long pstart = pi.pstart, pend = pi.pend;
   const int len = (int)(pend - pstart);
   if (len <= 0) return;
 
   // ---------------- producer state (warp 0, warp-uniform) ----------------
-  Cursor cur;
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
-  if (warp == 0) cursor_from_table(cur, p, pstart, a);
 
   auto issue = [&](int j) {
     if (cur.s != w_seq || cur.blk < w_base || cur.blk >= w_base + 32) {
@@ -490,6 +490,10 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   a.max_blocks = max_blocks;
   a.cum = reinterpret_cast<int32_t*>(ws + wl.cum);
   a.ctx_eff = reinterpret_cast<int32_t*>(ws + wl.ctx);
+  a.ctx_raw = context_lens;
+  a.max_ctx = max_blocks * block_size;
+  a.block_size = block_size;
+  a.inline_plan = batch <= kInlinePlanSeqs;
   a.pieces = reinterpret_cast<int4*>(ws + wl.pieces);
   a.batch = batch;
   a.n_h = n_h;
@@ -505,7 +509,8 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   a.stages = v->stages;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_plan(context_lens, batch, max_blocks * block_size, block_size, a, v->P, st);
+  cudaError_t e = a.inline_plan ? cudaSuccess
+                                : launch_plan(context_lens, batch, max_blocks * block_size, block_size, a, v->P, st);
   if (e == cudaSuccess) {
     void* kargs[] = {&tmk, &tmv, &a};
     e = launch_pdl(v->fn, dim3(v->P), dim3(v->warps * 32), v->smem, st, kargs);

@@ -33,6 +33,10 @@ struct DecodeArgs {
   float* ws_o;                   // [parts][G][D] unnormalised partial outputs
   int32_t* err;
   int stages;
+  // Without a plan kernel (batch <= kInlinePlanSeqs) the kernels read the raw context
+  // lengths and clamp them to [0, max_ctx] themselves.
+  const int32_t* ctx_raw;
+  int max_ctx, block_size, inline_plan;
   // INT4 cache (unused by the bf16 kernel)
   const uint8_t* k_codes;
   const uint8_t* v_codes;
@@ -90,6 +94,85 @@ __device__ __forceinline__ void cursor_from_table(Cursor& c, int p, long long ps
   c.seg_start = pstart - c.blk;
 }
 
+constexpr int kInlinePlanSeqs = 1024;
+
+__device__ __forceinline__ int clamp_ctx(int c, int max_ctx) { return c < 0 ? 0 : (c > max_ctx ? max_ctx : c); }
+
+// The part of the line a CTA owns, computed by one whole warp (every lane gets the same
+// values).  With the plan kernel: from its prefix sums and the start-cursor table.
+// Without it: the warp loads all context lengths (32 per chunk, every load issued before
+// any is used), sums the blocks, and warp 0 scans the chunks to find its start cursor.
+struct PieceInfo {
+  long long W, pstart, pend;
+  int P;
+};
+
+__device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_launch, bool want_cursor, Cursor& cur,
+                                            PieceInfo& pi) {
+  const int lane = threadIdx.x & 31;
+  if (!a.inline_plan) {
+    pi.W = (long long)a.n_kv * a.cum[a.batch];
+    pi.P = effective_pieces(pi.W, P_launch);
+    pi.pstart = pi.W * p / pi.P;
+    pi.pend = pi.W * (p + 1) / pi.P;
+    if (want_cursor && p < pi.P && pi.pstart < pi.pend) cursor_from_table(cur, p, pi.pstart, a);
+    return;
+  }
+  constexpr int MAXC = kInlinePlanSeqs / 32;
+  const int nch = (a.batch + 31) / 32;
+  int cv[MAXC];
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) {
+    const int s = c * 32 + lane;
+    cv[c] = (c < nch && s < a.batch) ? a.ctx_raw[s] : 0;
+  }
+  long long total = 0;
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) {
+    if (c >= nch) break;
+    bad |= cv[c] < 0 || cv[c] > a.max_ctx;
+    cv[c] = clamp_ctx(cv[c], a.max_ctx);
+    int nb = (cv[c] + a.block_size - 1) / a.block_size;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) nb += __shfl_xor_sync(FULL_MASK, nb, o);
+    total += nb;
+  }
+  if (__any_sync(FULL_MASK, bad) && lane == 0 && blockIdx.x == 0 && threadIdx.x == 0) set_err(a.err, PKV_DEV_BAD_CTX);
+  pi.W = (long long)a.n_kv * total;
+  pi.P = effective_pieces(pi.W, P_launch);
+  pi.pstart = pi.W * p / pi.P;
+  pi.pend = pi.W * (p + 1) / pi.P;
+  if (!want_cursor || p >= pi.P || pi.pstart >= pi.pend) return;
+  long long before = 0;                                      // blocks of earlier chunks
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) {
+    if (c >= nch) break;
+    const int nb = (cv[c] + a.block_size - 1) / a.block_size;
+    int incl = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long lo = (long long)a.n_kv * (before + incl - nb), hi = (long long)a.n_kv * (before + incl);
+    const unsigned hit = __ballot_sync(FULL_MASK, nb > 0 && lo <= pi.pstart && pi.pstart < hi);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const long long lo_s = __shfl_sync(FULL_MASK, lo, src);
+      cur.s = c * 32 + src;
+      cur.nb = __shfl_sync(FULL_MASK, nb, src);
+      cur.ctx = __shfl_sync(FULL_MASK, cv[c], src);
+      const long long off = pi.pstart - lo_s;
+      cur.g = (int)(off / cur.nb);
+      cur.blk = (int)(off % cur.nb);
+      cur.seg_start = pi.pstart - cur.blk;
+      return;
+    }
+    before += __shfl_sync(FULL_MASK, incl, 31);
+  }
+}
+
 // Advance by one position; only called while positions remain, so a non-empty
 // sequence lies ahead when the kv heads of the current one are exhausted.
 __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
@@ -98,6 +181,14 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
   c.blk = 0;
   if (++c.g < a.n_kv) return;
   c.g = 0;
+  if (a.inline_plan) {
+    do {
+      ++c.s;
+      c.ctx = clamp_ctx(a.ctx_raw[c.s], a.max_ctx);
+      c.nb = (c.ctx + a.block_size - 1) / a.block_size;
+    } while (c.nb == 0 && c.s < a.batch - 1);
+    return;
+  }
   do {
     ++c.s;
     c.nb = a.cum[c.s + 1] - a.cum[c.s];

@@ -178,9 +178,39 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
   long long W = 0, seg = 0;
   if (live) {
     s = row / a.n_h; h = row % a.n_h; g = h / a.G; hl = h % a.G;
-    const int c0 = a.cum[s];
-    nb = a.cum[s + 1] - c0;
-    W = (long long)a.n_kv * a.cum[a.batch];
+    long long c0 = 0, total = 0;
+    if (a.inline_plan) {
+      // blocks of the sequences before s, of s, and of all, from the raw context lengths
+      constexpr int MAXC = kInlinePlanSeqs / 32;
+      const int nch = (a.batch + 31) / 32;
+      int cv[MAXC];
+#pragma unroll
+      for (int c = 0; c < MAXC; ++c) {
+        const int sq = c * 32 + lane;
+        cv[c] = (c < nch && sq < a.batch) ? a.ctx_raw[sq] : 0;
+      }
+#pragma unroll
+      for (int c = 0; c < MAXC; ++c) {
+        if (c >= nch) break;
+        const int sq = c * 32 + lane;
+        const int b = (clamp_ctx(cv[c], a.max_ctx) + a.block_size - 1) / a.block_size;
+        int mine = sq == s ? b : 0, prev = sq < s ? b : 0, all = b;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          mine += __shfl_xor_sync(FULL_MASK, mine, o);
+          prev += __shfl_xor_sync(FULL_MASK, prev, o);
+          all += __shfl_xor_sync(FULL_MASK, all, o);
+        }
+        nb += mine;
+        c0 += prev;
+        total += all;
+      }
+    } else {
+      c0 = a.cum[s];
+      nb = a.cum[s + 1] - a.cum[s];
+      total = a.cum[a.batch];
+    }
+    W = (long long)a.n_kv * total;
     P = effective_pieces(W, P);
     if (nb > 0) {
       const long long seg_start = (long long)a.n_kv * c0 + (long long)g * nb;
