@@ -181,13 +181,18 @@ def recorded_traffic(workload: str):
 # ---------------------------------------------------------------------------------------------
 def l2_policy(step_bytes, flush_buf):
     """Steps that stream at least 4x the L2 need no flush (the data a step leaves in L2 is
-    the tail of each CTA's piece, which the next step reaches last, after evicting it);
-    smaller steps get a flush (a write of 2x L2) between timed steps.  A write flush leaves
-    L2 full of dirty lines whose write-back the next step would pay for, so it is only used
-    where the inputs alone would not defeat L2."""
+    the tail of each CTA's piece, which the next step reaches last, after evicting it).
+    Smaller steps get a flush between timed steps: a write of 2x L2, then a read of it, so
+    the written lines are evicted (and written back) before the timed step rather than
+    during it; the step starts from a cold, clean L2."""
     if step_bytes >= 4 * L2_BYTES:
         return (lambda: None), "no flush: each step streams >= 4x the L2 (inputs larger than L2)"
-    return (lambda: flush_buf.zero_()), "L2 flushed between steps (write of 2x L2, outside the events)"
+
+    def flush():
+        flush_buf.zero_()
+        flush_buf.view(torch.int32).max()
+
+    return flush, "L2 flushed between steps (write of 2x L2, then read back; outside the events)"
 
 
 def time_steps(step, K, W, flush, stream):

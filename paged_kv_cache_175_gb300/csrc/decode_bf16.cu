@@ -383,19 +383,12 @@ static Bf16Variant make_variant() {
   Bf16Variant v;
   v.fn = (const void*)decode_bf16_kernel<D, BS, NH, MT>;
   v.stage_bytes = Bf16Tile<D, BS>::STAGE;
-  v.stages = ring_stages(v.stage_bytes, "PKV_STAGES_BF16");
+  v.stages = ring_stages(v.stage_bytes, 24576, "PKV_STAGES_BF16");
   v.smem = bf16_smem_bytes<D, BS>(v.stages);
   v.warps = MT;
   v.P = 0;
   return v;
 }
-
-int mt_for_group(int G) { return G <= 16 ? 1 : (G <= 32 ? 2 : 4); }
-
-// Head tiling of a group: G <= 8 -> one warp with one 8-head n-tile; otherwise warps of
-// two 8-head n-tiles (16 heads each), ceil(G / 16) of them rounded up to 1, 2 or 4.
-// Variant index: 0 (NH 1, MT 1), 1 (2, 1), 2 (2, 2), 3 (2, 4).
-static int bf16_tiling(int G) { return G <= 8 ? 0 : (G <= 16 ? 1 : (G <= 32 ? 2 : 3)); }
 
 static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   // One table per process; the library drives one device per process.
@@ -427,7 +420,7 @@ static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
 }
 
 int bf16_pieces(int D, int BS, int G) {
-  Bf16Variant* v = lookup_bf16(D, BS, bf16_tiling(G));
+  Bf16Variant* v = lookup_bf16(D, BS, head_tiling(G));
   return v ? v->P : 0;
 }
 
@@ -467,7 +460,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
     return PKV_EINVAL;
   if ((long long)max_blocks * block_size > 0x7fffffffLL) return PKV_ERANGE;
   const int G = n_h / n_kv;
-  Bf16Variant* v = lookup_bf16(head_dim, block_size, bf16_tiling(G));
+  Bf16Variant* v = lookup_bf16(head_dim, block_size, head_tiling(G));
   if (!v) {
     record_cuda_error(cudaGetLastError());
     return PKV_ECUDA;

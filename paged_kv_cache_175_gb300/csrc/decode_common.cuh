@@ -94,7 +94,7 @@ __device__ __forceinline__ void cursor_from_table(Cursor& c, int p, long long ps
   c.seg_start = pstart - c.blk;
 }
 
-constexpr int kInlinePlanSeqs = 1024;
+constexpr int kInlinePlanSeqs = 256;
 
 __device__ __forceinline__ int clamp_ctx(int c, int max_ctx) { return c < 0 ? 0 : (c > max_ctx ? max_ctx : c); }
 
@@ -130,13 +130,14 @@ __device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_la
   bool bad = false;
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
-    if (c >= nch) break;
-    bad |= cv[c] < 0 || cv[c] > a.max_ctx;
-    cv[c] = clamp_ctx(cv[c], a.max_ctx);
-    int nb = (cv[c] + a.block_size - 1) / a.block_size;
+    if (c < nch) {
+      bad |= cv[c] < 0 || cv[c] > a.max_ctx;
+      cv[c] = clamp_ctx(cv[c], a.max_ctx);
+      int nb = (cv[c] + a.block_size - 1) / a.block_size;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) nb += __shfl_xor_sync(FULL_MASK, nb, o);
-    total += nb;
+      for (int o = 16; o; o >>= 1) nb += __shfl_xor_sync(FULL_MASK, nb, o);
+      total += nb;
+    }
   }
   if (__any_sync(FULL_MASK, bad) && lane == 0 && blockIdx.x == 0 && threadIdx.x == 0) set_err(a.err, PKV_DEV_BAD_CTX);
   pi.W = (long long)a.n_kv * total;
@@ -145,9 +146,10 @@ __device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_la
   pi.pend = pi.W * (p + 1) / pi.P;
   if (!want_cursor || p >= pi.P || pi.pstart >= pi.pend) return;
   long long before = 0;                                      // blocks of earlier chunks
+  bool found = false;
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
-    if (c >= nch) break;
+    if (c >= nch || found) continue;
     const int nb = (cv[c] + a.block_size - 1) / a.block_size;
     int incl = nb;
 #pragma unroll
@@ -167,7 +169,8 @@ __device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_la
       cur.g = (int)(off / cur.nb);
       cur.blk = (int)(off % cur.nb);
       cur.seg_start = pi.pstart - cur.blk;
-      return;
+      found = true;
+      continue;
     }
     before += __shfl_sync(FULL_MASK, incl, 31);
   }
@@ -203,11 +206,15 @@ cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t
 cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void** args);
 int device_sm_count();
-// Stages of the shared-memory ring for a stage of `stage_bytes`: about 24 KB of ring per
-// CTA, at least 2 and at most 8; the environment variable `env` (an integer 2..16)
-// overrides it for tuning.
-int ring_stages(size_t stage_bytes, const char* env);
-int mt_for_group(int G);           // consumer warps (16 heads each) per CTA
+// Stages of the shared-memory ring for a stage of `stage_bytes`: about `ring_bytes` of
+// ring per CTA, at least 2 and at most 8; the environment variable `env` (an integer
+// 2..16) overrides it for tuning.  A small ring leaves room for more resident CTAs,
+// which these latency-bound kernels need more than deep prefetch (measured: 24 KB for
+// the bf16 cache, 16 KB for INT4).
+int ring_stages(size_t stage_bytes, size_t ring_bytes, const char* env);
+// Head tiling of a group for the attention kernels: 0 = one warp of 8 heads (G <= 8);
+// 1 / 2 / 3 = 1 / 2 / 4 warps of 16 heads (G <= 16 / 32 / 64).
+inline int head_tiling(int G) { return G <= 8 ? 0 : (G <= 16 ? 1 : (G <= 32 ? 2 : 3)); }
 int bf16_pieces(int D, int BS, int G);
 int int4_pieces(int D, int BS, int G);
 void record_cuda_error(cudaError_t e);

@@ -52,12 +52,12 @@ int encode_tensor_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64
   return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-int ring_stages(size_t stage_bytes, const char* env) {
+int ring_stages(size_t stage_bytes, size_t ring_bytes, const char* env) {
   if (const char* e = getenv(env)) {
     const int v = atoi(e);
     if (v >= 2 && v <= 16) return v;
   }
-  const int st = (int)(24576 / stage_bytes);
+  const int st = (int)(ring_bytes / stage_bytes);
   return st < 2 ? 2 : (st > 8 ? 8 : st);
 }
 
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
       }
 #pragma unroll
       for (int c = 0; c < MAXC; ++c) {
-        if (c >= nch) break;
+        if (c >= nch) continue;
         const int sq = c * 32 + lane;
         const int b = (clamp_ctx(cv[c], a.max_ctx) + a.block_size - 1) / a.block_size;
         int mine = sq == s ? b : 0, prev = sq < s ? b : 0, all = b;

@@ -190,34 +190,36 @@ __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a
 // ---------------------------------------------------------------------------------------------
 // Decode attention over the INT4 cache.
 //
-// Stage layout for one (block, kv head): K codes [BS][D/2], V codes [BS][D/2], K meta
-// [2][D] fp16, V meta [BS][2] fp16, and room for a bf16 K tail [BS][D] used only by a
-// sequence's unfinished last block.  Each piece is one 1-D bulk copy.
+// Same partition, producer and token-major tiles as the bf16 kernel.  A stage holds one
+// (block, kv head): K codes [BS][D/2], V codes [BS][D/2], K meta [2][D] fp16 and V meta
+// [BS][2] fp16, each one 1-D bulk copy.  A sequence's unfinished last block has no K
+// codes: its K rows are read from the bf16 tail straight from L2 (the producer
+// prefetches them when the segment starts and again when it issues the block), so the
+// ring holds no tail space.
 //
-// Q K^T uses fp16 mma.  The channel order inside a k-step is chosen so each thread's
-// B-fragment comes from one 16-byte load of its token row: thread t of a quad owns
-// channels [t*D/4, (t+1)*D/4); k-step ks takes word ks/2 and, inside it, channel pairs
-// (0,1),(2,3) or (4,5),(6,7).  The A-fragment (q, converted to fp16 once per segment
-// part) uses the same channel order.  Dequantization x^ = fp16(code * s + m) runs on
-// half2 pairs: the code pair is unpacked into 1024 + code by a mask-and-or, 1024 is
-// subtracted (exact), then one fused multiply-add with the channel pair's (s, m) rounds
-// the exact value once, as the format defines it.
+// S^T = K^ Q^T uses fp16 mma.  The channel order inside a k-step is chosen so each
+// thread's A-fragment rows come from one 16-byte load of a token row: thread t of a quad
+// owns channels [t*D/4, (t+1)*D/4); k-step ks takes word ks/2 and, inside it, channel
+// pairs (0,1),(2,3) or (4,5),(6,7); Q^T (converted to fp16 once per segment part) uses
+// the same order.  Dequantization x^ = fp16(code * s + m) runs on half2 pairs: the code
+// pair is unpacked into 1024 + code by a mask-and-or, 1024 is subtracted (exact), then
+// one fused multiply-add with the pair's (s, m) rounds the exact value once, as the
+// format defines it.
 //
-// P V uses fp16 mma with P carried as an fp16 high part plus an fp16 low part (two mma
-// per tile).  Thread u of a group of four owns output channels [u*D/8, (u+1)*D/8) as
-// B-fragment columns; a byte of a V code word pairs the same nibble of two token rows
-// (byte permute), giving a half2 of two tokens of one channel, scaled by the two
+// O^T = V^T P^T uses fp16 mma with P carried as an fp16 high part plus an fp16 low part.
+// Thread g of the eight row groups owns channels [g*D/8, (g+1)*D/8); a byte of a V code
+// word, permuted together from two token rows, gives a half2 of two tokens of one channel
+// (the even nibble for fragment row g, the odd one for row g+8), scaled by the two
 // tokens' (s, m).
 template <int D, int BS>
 struct Int4Tile {
-  static constexpr int KC = 0;
-  static constexpr int VC = BS * D / 2;
-  static constexpr int KM = BS * D;
-  static constexpr int VM = BS * D + 4 * D;
-  static constexpr int KT = (BS * D + 4 * D + 4 * BS + 15) / 16 * 16;
-  static constexpr int STAGE = (KT + BS * D * 2 + 127) / 128 * 128;
+  static constexpr int KC = 0;                              // K codes [BS][D/2]
+  static constexpr int VC = BS * D / 2;                     // V codes [BS][D/2]
+  static constexpr int KM = BS * D;                         // K meta [2][D] fp16
+  static constexpr int VM = BS * D + 4 * D;                 // V meta [BS][2] fp16
+  static constexpr int STAGE = (BS * D + 4 * D + 4 * BS + 127) / 128 * 128;
   static constexpr int FULL_BYTES = BS * D + 4 * D + 4 * BS;          // codes + metadata
-  static constexpr int TAIL_BYTES = BS * D / 2 + 4 * BS + 2 * BS * D;   // V codes + V meta + K tail
+  static constexpr int TAIL_BYTES = BS * D / 2 + 4 * BS;              // V codes + V meta
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -236,21 +238,26 @@ __device__ __forceinline__ uint32_t dq2(uint32_t h1024, uint32_t s2, uint32_t m2
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) { return pack_f16(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ uint32_t mask_pair_h(uint32_t b, int t, int ntok) {
+  return b & ((t < ntok ? 0x0000ffffu : 0u) | (t + 1 < ntok ? 0xffff0000u : 0u));
+}
 
 template <int D, int BS>
 __host__ __device__ constexpr size_t int4_smem_bytes(int stages) {
   return 1024 + (size_t)stages * (Int4Tile<D, BS>::STAGE + 16 + 16);
 }
 
-template <int D, int BS, int MT>
+template <int D, int BS, int NH, int MT>
 __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a) {
   using T = Int4Tile<D, BS>;
-  constexpr int NT = BS / 8;
-  constexpr int KS = D / 16;
-  constexpr int DN = D / 8;
+  constexpr int TT = BS / 16;       // 16-token tiles per block
+  constexpr int KS = D / 16;        // k-steps of K Q^T
+  constexpr int MD = D / 16;        // 16-channel m-tiles of O^T
+  constexpr int HW = 8 * NH;        // heads per warp
   constexpr int KW = D / 32;        // K code words per thread per token row
-  constexpr int CB = D / 4;         // K channels per thread (QK k-slots)
-  constexpr int CV = D / 8;         // V channels per thread (PV columns)
+  constexpr int CB = D / 4;         // K channels per thread (k-slots of the QK fragments)
+  constexpr int CV = D / 8;         // V channels per thread (rows of the V^T fragments)
+  constexpr int VW = CV / 8;        // V code words per thread per token row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + S);
   uint64_t* empty = full + S;
   __shared__ volatile int abort_flag;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3, u = lane >> 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3, gid = lane >> 2;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -315,39 +322,49 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
       const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
       if (ok) flags |= F_VALID; else set_err(a.err, PKV_DEV_BAD_BLOCK);
       meta[slot] = make_int4(cur.s, cur.g, cur.blk, ntok | (flags << 8));
+      const char* tail = reinterpret_cast<const char*>(a.k_tail + ((size_t)cur.s * a.n_kv + cur.g) * BS * D);
       if (ok && ok_wait) {
         uint8_t* st = smem + (size_t)slot * T::STAGE;
         const size_t tile = (size_t)phys * a.n_kv + cur.g;
         if (ntok == BS) {
           mbar_arrive_expect_tx(&full[slot], T::FULL_BYTES);
           bulk_g2s(st + T::KC, a.k_codes + tile * (BS * D / 2), BS * D / 2, &full[slot], pol);
-          bulk_g2s(st + T::VC, a.v_codes + tile * (BS * D / 2), BS * D / 2, &full[slot], pol);
           bulk_g2s(st + T::KM, a.k_meta + tile * (2 * D), 4 * D, &full[slot], pol);
-          bulk_g2s(st + T::VM, a.v_meta + tile * (2 * BS), 4 * BS, &full[slot], pol);
         } else {
+          // the sequence's unfinished block: K comes from its bf16 tail (read by the
+          // consumers straight from L2), V from the codes
           mbar_arrive_expect_tx(&full[slot], T::TAIL_BYTES);
-          bulk_g2s(st + T::VC, a.v_codes + tile * (BS * D / 2), BS * D / 2, &full[slot], pol);
-          bulk_g2s(st + T::VM, a.v_meta + tile * (2 * BS), 4 * BS, &full[slot], pol);
-          bulk_g2s(st + T::KT, a.k_tail + ((size_t)cur.s * a.n_kv + cur.g) * BS * D, 2 * BS * D, &full[slot], pol);
+          for (int off = 0; off < 2 * BS * D; off += 128) prefetch_l2(tail + off);
         }
+        bulk_g2s(st + T::VC, a.v_codes + tile * (BS * D / 2), BS * D / 2, &full[slot], pol);
+        bulk_g2s(st + T::VM, a.v_meta + tile * (2 * BS), 4 * BS, &full[slot], pol);
       } else {
         mbar_arrive(&full[slot]);
       }
       if (flags & F_FIRST) {
         const char* qp = reinterpret_cast<const char*>(a.q) + ((size_t)cur.s * a.n_h + (size_t)cur.g * a.G) * D * 2;
         for (int off = 0; off < a.G * D * 2; off += 128) prefetch_l2(qp + off);
+        if (cur.ctx % BS)                                      // warm L2 with the tail early
+          for (int off = 0; off < 2 * BS * D; off += 128) prefetch_l2(tail + off);
       }
     }
     if (j + 1 < len) cursor_next(cur, a);
   };
 
-  uint32_t qa[KS][4];
-  float o[DN][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int hl0 = warp * 16 + u, hl1 = hl0 + 8;
-  const bool v0 = hl0 < a.G, v1 = hl1 < a.G;
+  // ---------------- consumer state (warp w: local heads [w*HW, (w+1)*HW)) ----------------
+  // Token-major tiles as in the bf16 kernel.  K^ is the A operand (tokens x channels); its
+  // channel order inside a k-step follows the code words: thread tig owns channels
+  // [tig*CB, (tig+1)*CB); k-step ks takes word ks/2 and, in it, the pairs (0,1),(2,3) or
+  // (4,5),(6,7) -- Q^T's B fragments use the same order.  V^T is the A operand of the
+  // second product (channels x tokens): thread gid owns channels [gid*CV, (gid+1)*CV);
+  // byte k of code word w of two token rows gives the m-tile 4w+k rows gid (even nibble)
+  // and gid+8 (odd nibble).
+  uint32_t qb[KS][NH][2];
+  float o[MD][NH][4];
+  float m[NH][2], l[NH][2];
+  const int hw0 = warp * HW;
   const int cb = tig * CB;           // first K channel of this thread
-  const int cv = u * CV;             // first V output column channel of this thread
+  const int cv = gid * CV;           // first V channel of this thread
 
   if (warp == 0) {
     const int pre = len < S ? len : S;
@@ -365,32 +382,39 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
     consumed = j + 1;
     const int4 mt = meta[slot];
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = mt.w >> 8;
+    const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;
 
     if (flags & F_FIRST) {
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(a.q) + ((size_t)s * a.n_h + (size_t)g * a.G + hl0) * (D / 2);
-      const uint32_t* q1 = q0 + 8 * (D / 2);
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int w = (cb + 8 * (ks >> 1) + 4 * (ks & 1)) >> 1;   // word of channel pair (c0, c0+1)
-        qa[ks][0] = v0 ? bf2_to_h2(__ldg(q0 + w)) : 0u;
-        qa[ks][1] = v1 ? bf2_to_h2(__ldg(q1 + w)) : 0u;
-        qa[ks][2] = v0 ? bf2_to_h2(__ldg(q0 + w + 1)) : 0u;
-        qa[ks][3] = v1 ? bf2_to_h2(__ldg(q1 + w + 1)) : 0u;
+      for (int nh = 0; nh < NH; ++nh) {
+        const int hl = hw0 + nh * 8 + gid;
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q) + (qrow0 + hl) * (D / 2);
+        const bool ok = hl < a.G;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int w = (cb >> 1) + 4 * (ks >> 1) + 2 * (ks & 1);   // channel pair cb + 2*pr
+          qb[ks][nh][0] = ok ? bf2_to_h2(__ldg(qp + w)) : 0u;
+          qb[ks][nh][1] = ok ? bf2_to_h2(__ldg(qp + w + 1)) : 0u;
+        }
+        m[nh][0] = m[nh][1] = -INFINITY;
+        l[nh][0] = l[nh][1] = 0.f;
+#pragma unroll
+        for (int md = 0; md < MD; ++md) o[md][nh][0] = o[md][nh][1] = o[md][nh][2] = o[md][nh][3] = 0.f;
       }
-#pragma unroll
-      for (int n = 0; n < DN; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
     }
 
     if (flags & F_VALID) {
       const uint8_t* st = smem + (size_t)slot * T::STAGE;
-      const bool tailblk = ntok < BS;
-      float sc[NT][4];
+      const bool partial = ntok < BS;
+      // ---- S^T = K^ Q^T (fp16 in, fp32 accumulate; even / odd k-steps in two accumulators) ----
+      float sc[TT][NH][4], sx[TT][NH][4];
 #pragma unroll
-      for (int n = 0; n < NT; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-      // ---- S = Q K^T ----
-      if (!tailblk) {
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[t][nh][i] = sx[t][nh][i] = 0.f;
+      if (!partial) {
         uint32_t s2[CB / 2], m2[CB / 2];                          // (s, m) of channel pairs cb + 2k
         const uint4* kms = reinterpret_cast<const uint4*>(st + T::KM + cb * 2);
         const uint4* kmm = reinterpret_cast<const uint4*>(st + T::KM + 2 * D + cb * 2);
@@ -401,125 +425,161 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
           m2[4 * k4] = b4.x; m2[4 * k4 + 1] = b4.y; m2[4 * k4 + 2] = b4.z; m2[4 * k4 + 3] = b4.w;
         }
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          uint32_t wd[KW];
-          const uint8_t* rowp = st + T::KC + (n * 8 + u) * (D / 2) + tig * (D / 8);
+        for (int t = 0; t < TT; ++t) {
+          uint32_t w0[KW], w1[KW];                                // code words of rows gid, gid+8
+          const uint8_t* r0 = st + T::KC + (t * 16 + gid) * (D / 2) + tig * (D / 8);
+          const uint8_t* r1 = r0 + 8 * (D / 2);
           if constexpr (KW == 4) {
-            const uint4 t4 = *reinterpret_cast<const uint4*>(rowp);
-            wd[0] = t4.x; wd[1] = t4.y; wd[2] = t4.z; wd[3] = t4.w;
+            const uint4 x = *reinterpret_cast<const uint4*>(r0), y = *reinterpret_cast<const uint4*>(r1);
+            w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
+            w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
           } else {
-            const uint2 t2 = *reinterpret_cast<const uint2*>(rowp);
-            wd[0] = t2.x; wd[1] = t2.y;
+            const uint2 x = *reinterpret_cast<const uint2*>(r0), y = *reinterpret_cast<const uint2*>(r1);
+            w0[0] = x.x; w0[1] = x.y;
+            w1[0] = y.x; w1[1] = y.y;
           }
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
-            const int w = ks >> 1, hsel = 2 * (ks & 1);         // pairs h_hsel, h_hsel+1 of word w
-            const uint32_t x0 = lop_nib(wd[w] >> (4 * hsel)), x1 = lop_nib(wd[w] >> (4 * hsel + 4));
-            const int pr = 4 * w + hsel;                         // channel pair index (cb + 2*pr)
-            const uint32_t b0 = dq2(x0, s2[pr], m2[pr]), b1 = dq2(x1, s2[pr + 1], m2[pr + 1]);
-            mma_f16(sc[n], qa[ks], b0, b1);
+            const int w = ks >> 1, hs = 2 * (ks & 1), pr = 4 * w + hs;
+            uint32_t ka[4];
+            ka[0] = dq2(lop_nib(w0[w] >> (4 * hs)), s2[pr], m2[pr]);
+            ka[1] = dq2(lop_nib(w1[w] >> (4 * hs)), s2[pr], m2[pr]);
+            ka[2] = dq2(lop_nib(w0[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
+            ka[3] = dq2(lop_nib(w1[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+              if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+              else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+            }
           }
         }
       } else {
+        // unfinished block: K rows from the bf16 tail in global memory (prefetched to L2)
+        const uint4* tl = reinterpret_cast<const uint4*>(a.k_tail + ((size_t)s * a.n_kv + g) * BS * D);
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const uint4* rowp = reinterpret_cast<const uint4*>(st + T::KT + (size_t)(n * 8 + u) * D * 2 + cb * 2);
-          uint32_t wd[CB / 2];
+        for (int t = 0; t < TT; ++t) {
+          uint32_t w0[CB / 2], w1[CB / 2];                        // bf16 pairs of channels cb + 2k
+          const uint4* r0 = tl + ((size_t)(t * 16 + gid) * D + cb) / 8;
+          const uint4* r1 = r0 + D;                               // 8 rows further (D / 8 uint4 per row)
 #pragma unroll
           for (int k4 = 0; k4 < CB / 8; ++k4) {
-            const uint4 t4 = rowp[k4];
-            wd[4 * k4] = t4.x; wd[4 * k4 + 1] = t4.y; wd[4 * k4 + 2] = t4.z; wd[4 * k4 + 3] = t4.w;
+            const uint4 x = __ldg(r0 + k4), y = __ldg(r1 + k4);
+            w0[4 * k4] = x.x; w0[4 * k4 + 1] = x.y; w0[4 * k4 + 2] = x.z; w0[4 * k4 + 3] = x.w;
+            w1[4 * k4] = y.x; w1[4 * k4 + 1] = y.y; w1[4 * k4 + 2] = y.z; w1[4 * k4 + 3] = y.w;
           }
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             const int pr = 4 * (ks >> 1) + 2 * (ks & 1);
-            mma_f16(sc[n], qa[ks], bf2_to_h2(wd[pr]), bf2_to_h2(wd[pr + 1]));
+            uint32_t ka[4];
+            ka[0] = bf2_to_h2(w0[pr]);
+            ka[1] = bf2_to_h2(w1[pr]);
+            ka[2] = bf2_to_h2(w0[pr + 1]);
+            ka[3] = bf2_to_h2(w1[pr + 1]);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+              if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+              else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+            }
           }
         }
       }
-      // ---- online softmax (base 2) ----
-      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
+      for (int t = 0; t < TT; ++t)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tok = n * 8 + 2 * tig + e;
-          float x0 = sc[n][e] * a.scale_log2, x1 = sc[n][2 + e] * a.scale_log2;
-          if (tok >= ntok) x0 = x1 = -INFINITY;
-          sc[n][e] = x0;
-          sc[n][2 + e] = x1;
-          mx0 = fmaxf(mx0, x0);
-          mx1 = fmaxf(mx1, x1);
-        }
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(FULL_MASK, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(FULL_MASK, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float rs0 = 0.f, rs1 = 0.f;
+        for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
+          for (int i = 0; i < 4; ++i) sc[t][nh][i] += sx[t][nh][i];
+      // ---- online softmax over tokens (rows), per head (column), base 2 ----
+      float al[NH][2];
+      bool rescale = false;
+#pragma unroll
+      for (int nh = 0; nh < NH; ++nh) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          sc[n][e] = ex2(sc[n][e] - mn0);
-          sc[n][2 + e] = ex2(sc[n][2 + e] - mn1);
-          rs0 += sc[n][e];
-          rs1 += sc[n][2 + e];
-        }
-      }
-      l0 = l0 * al0 + rs0;
-      l1 = l1 * al1 + rs1;
-      if (__any_sync(FULL_MASK, al0 != 1.f || al1 != 1.f)) {
+          float mx = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < DN; ++n) {
-          o[n][0] *= al0; o[n][1] *= al0; o[n][2] *= al1; o[n][3] *= al1;
+          for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int tok = t * 16 + gid + 8 * r;
+              float x = sc[t][nh][2 * r + e] * a.scale_log2;
+              if (tok >= ntok) x = -INFINITY;
+              sc[t][nh][2 * r + e] = x;
+              mx = fmaxf(mx, x);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+          const float mn = fmaxf(m[nh][e], mx);
+          al[nh][e] = ex2(m[nh][e] - mn);
+          rescale |= al[nh][e] != 1.f;
+          m[nh][e] = mn;
+          float rs = 0.f;
+#pragma unroll
+          for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float pv = ex2(sc[t][nh][2 * r + e] - mn);
+              sc[t][nh][2 * r + e] = pv;
+              rs += pv;
+            }
+          l[nh][e] = l[nh][e] * al[nh][e] + rs;
         }
       }
-      // ---- O += P V ----
+      if (__any_sync(FULL_MASK, rescale)) {
+#pragma unroll
+        for (int md = 0; md < MD; ++md)
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) {
+            o[md][nh][0] *= al[nh][0]; o[md][nh][1] *= al[nh][1];
+            o[md][nh][2] *= al[nh][0]; o[md][nh][3] *= al[nh][1];
+          }
+      }
+      // ---- O^T += V^T P^T (fp16, P as high + low) ----
       const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + T::VM);
 #pragma unroll
-      for (int kt = 0; kt < BS / 16; ++kt) {
-        uint32_t pa[4], pl[4];                                    // P = high + low, both fp16
+      for (int t = 0; t < TT; ++t) {
+        uint32_t bh[NH][2], bl[NH][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x = sc[2 * kt + (i >> 1)][(i & 1) * 2], y = sc[2 * kt + (i >> 1)][(i & 1) * 2 + 1];
-          pa[i] = pack_f16(x, y);
-          const __half2 h = *reinterpret_cast<const __half2*>(&pa[i]);
-          pl[i] = pack_f16(x - __low2float(h), y - __high2float(h));
-        }
-        const int t0 = kt * 16 + 2 * tig;                        // b0: tokens t0, t0+1; b1: t0+8, t0+9
+        for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float x = sc[t][nh][2 * r], y = sc[t][nh][2 * r + 1];
+            const uint32_t hi = pack_f16(x, y);
+            const __half2 h = *reinterpret_cast<const __half2*>(&hi);
+            const uint32_t lo = pack_f16(x - __low2float(h), y - __high2float(h));
+            bh[nh][r] = movmatrix_t(hi);
+            bl[nh][r] = movmatrix_t(lo);
+          }
+        const int t0 = t * 16 + 2 * tig;                         // a0/a1: tokens t0, t0+1; a2/a3: +8
         const uint32_t sA = prmt(vm[t0], vm[t0 + 1], 0x5410), mA = prmt(vm[t0], vm[t0 + 1], 0x7632);
         const uint32_t sB = prmt(vm[t0 + 8], vm[t0 + 9], 0x5410), mB = prmt(vm[t0 + 8], vm[t0 + 9], 0x7632);
         const uint8_t* vc = st + T::VC + cv / 2;
-        uint32_t ra[CV / 8], rb[CV / 8], rc[CV / 8], rd[CV / 8];   // code words of rows t0, t0+1, t0+8, t0+9
 #pragma unroll
-        for (int w = 0; w < CV / 8; ++w) {
-          ra[w] = *reinterpret_cast<const uint32_t*>(vc + (size_t)t0 * (D / 2) + 4 * w);
-          rb[w] = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 1) * (D / 2) + 4 * w);
-          rc[w] = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 8) * (D / 2) + 4 * w);
-          rd[w] = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 9) * (D / 2) + 4 * w);
-        }
-        const bool partial = ntok < BS;
-#pragma unroll
-        for (int w = 0; w < CV / 8; ++w) {
+        for (int w = 0; w < VW; ++w) {
+          const uint32_t ra = *reinterpret_cast<const uint32_t*>(vc + (size_t)t0 * (D / 2) + 4 * w);
+          const uint32_t rb = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 1) * (D / 2) + 4 * w);
+          const uint32_t rc = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 8) * (D / 2) + 4 * w);
+          const uint32_t rd = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 9) * (D / 2) + 4 * w);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t sel = (uint32_t)k | ((uint32_t)k << 4) | ((uint32_t)(4 + k) << 8) | ((uint32_t)(4 + k) << 12);
-            const uint32_t pAB = prmt(ra[w], rb[w], sel), pCD = prmt(rc[w], rd[w], sel);
+            const uint32_t pab = prmt(ra, rb, sel), pcd = prmt(rc, rd, sel);
+            uint32_t va[4];
+            va[0] = dq2(lop_nib(pab), sA, mA);                   // row gid   (even nibble), tokens t0, t0+1
+            va[1] = dq2(lop_nib(pab >> 4), sA, mA);              // row gid+8 (odd nibble)
+            va[2] = dq2(lop_nib(pcd), sB, mB);                   // row gid,   tokens t0+8, t0+9
+            va[3] = dq2(lop_nib(pcd >> 4), sB, mB);
+            if (partial) {
+              va[0] = mask_pair_h(va[0], t0, ntok);
+              va[1] = mask_pair_h(va[1], t0, ntok);
+              va[2] = mask_pair_h(va[2], t0 + 8, ntok);
+              va[3] = mask_pair_h(va[3], t0 + 8, ntok);
+            }
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              uint32_t b0 = dq2(lop_nib(pAB >> (4 * e)), sA, mA);
-              uint32_t b1 = dq2(lop_nib(pCD >> (4 * e)), sB, mB);
-              if (partial) {
-                b0 = b0 & ((t0 < ntok ? 0x0000ffffu : 0u) | (t0 + 1 < ntok ? 0xffff0000u : 0u));
-                b1 = b1 & ((t0 + 8 < ntok ? 0x0000ffffu : 0u) | (t0 + 9 < ntok ? 0xffff0000u : 0u));
-              }
-              mma_f16(o[8 * w + 2 * k + e], pa, b0, b1);
-              mma_f16(o[8 * w + 2 * k + e], pl, b0, b1);
+            for (int nh = 0; nh < NH; ++nh) {
+              mma_f16(o[4 * w + k][nh], va, bh[nh][0], bh[nh][1]);
+              mma_f16(o[4 * w + k][nh], va, bl[nh][0], bl[nh][1]);
             }
           }
         }
@@ -527,61 +587,53 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
     }
 
     if (flags & F_LAST) {
-      float L0 = l0 + __shfl_xor_sync(FULL_MASK, l0, 1);
-      L0 += __shfl_xor_sync(FULL_MASK, L0, 2);
-      float L1 = l1 + __shfl_xor_sync(FULL_MASK, l1, 1);
-      L1 += __shfl_xor_sync(FULL_MASK, L1, 2);
-      const bool whole = flags & F_WHOLE;
-      const float i0 = whole ? (L0 > 0.f ? 1.f / L0 : 0.f) : 1.f, i1 = whole ? (L1 > 0.f ? 1.f / L1 : 0.f) : 1.f;
-      // Column n-slot 2*tig + e of n-tile nt holds channel (2*tig+e)*CV + 8*(nt/8) + channel_of(nt%8).
+      float L[NH][2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float r0v[CV], r1v[CV];
+      for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-        for (int c = 0; c < CV; ++c) {
-          const int nt = 8 * (c >> 3) + nibble_of(c & 7);
-          r0v[c] = o[nt][e] * i0;
-          r1v[c] = o[nt][2 + e] * i1;
+        for (int e = 0; e < 2; ++e) {
+          float x = l[nh][e];
+          x += __shfl_xor_sync(FULL_MASK, x, 4);
+          x += __shfl_xor_sync(FULL_MASK, x, 8);
+          x += __shfl_xor_sync(FULL_MASK, x, 16);
+          L[nh][e] = x;
         }
-        const int c0 = (2 * tig + e) * CV;
-        if (whole) {
-          const size_t row0 = (size_t)s * a.n_h + (size_t)g * a.G + hl0;
-          if (a.out_f32) {
-            float* out0 = reinterpret_cast<float*>(a.out) + row0 * D + c0;
+      const bool whole = flags & F_WHOLE;
+      const long long part = (long long)s * a.n_kv + g + p;
 #pragma unroll
-            for (int c = 0; c < CV; c += 4) {
-              if (v0) *reinterpret_cast<float4*>(out0 + c) = make_float4(r0v[c], r0v[c + 1], r0v[c + 2], r0v[c + 3]);
-              if (v1) *reinterpret_cast<float4*>(out0 + 8 * D + c) = make_float4(r1v[c], r1v[c + 1], r1v[c + 2], r1v[c + 3]);
+      for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hl = hw0 + nh * 8 + 2 * tig + e;
+          if (hl >= a.G) continue;
+          const float inv = whole ? (L[nh][e] > 0.f ? 1.f / L[nh][e] : 0.f) : 1.f;
+          // m-tile md rows gid / gid+8 hold channel cv + 8*(md/4) + channel_of(2*(md%4) + 0 / 1)
+          if (whole) {
+            const size_t base = (qrow0 + hl) * D + cv;
+#pragma unroll
+            for (int md = 0; md < MD; ++md) {
+              const int c0 = 8 * (md >> 2) + channel_of(2 * (md & 3)), c1 = 8 * (md >> 2) + channel_of(2 * (md & 3) + 1);
+              if (a.out_f32) {
+                float* out = reinterpret_cast<float*>(a.out) + base;
+                out[c0] = o[md][nh][e] * inv;
+                out[c1] = o[md][nh][2 + e] * inv;
+              } else {
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + base;
+                out[c0] = __float2bfloat16_rn(o[md][nh][e] * inv);
+                out[c1] = __float2bfloat16_rn(o[md][nh][2 + e] * inv);
+              }
             }
           } else {
-            uint32_t* out0 = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row0 * D + c0);
+            float* wo = a.ws_o + ((size_t)part * a.G + hl) * D + cv;
 #pragma unroll
-            for (int c = 0; c < CV; c += 8) {
-              if (v0)
-                *reinterpret_cast<uint4*>(out0 + c / 2) =
-                    make_uint4(pack_bf16(r0v[c], r0v[c + 1]), pack_bf16(r0v[c + 2], r0v[c + 3]),
-                               pack_bf16(r0v[c + 4], r0v[c + 5]), pack_bf16(r0v[c + 6], r0v[c + 7]));
-              if (v1)
-                *reinterpret_cast<uint4*>(out0 + 4 * D + c / 2) =
-                    make_uint4(pack_bf16(r1v[c], r1v[c + 1]), pack_bf16(r1v[c + 2], r1v[c + 3]),
-                               pack_bf16(r1v[c + 4], r1v[c + 5]), pack_bf16(r1v[c + 6], r1v[c + 7]));
+            for (int md = 0; md < MD; ++md) {
+              wo[8 * (md >> 2) + channel_of(2 * (md & 3))] = o[md][nh][e];
+              wo[8 * (md >> 2) + channel_of(2 * (md & 3) + 1)] = o[md][nh][2 + e];
             }
-          }
-        } else {
-          const long long part = (long long)s * a.n_kv + g + p;
-          float* wo = a.ws_o + (size_t)part * a.G * D + c0;
-#pragma unroll
-          for (int c = 0; c < CV; c += 4) {
-            if (v0) *reinterpret_cast<float4*>(wo + (size_t)hl0 * D + c) = make_float4(r0v[c], r0v[c + 1], r0v[c + 2], r0v[c + 3]);
-            if (v1) *reinterpret_cast<float4*>(wo + (size_t)hl1 * D + c) = make_float4(r1v[c], r1v[c + 1], r1v[c + 2], r1v[c + 3]);
+            if (gid == 0)
+              *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl) * 2) = make_float2(m[nh][e], L[nh][e]);
           }
         }
-      }
-      if (!whole && tig == 0) {
-        const long long part = (long long)s * a.n_kv + g + p;
-        if (v0) *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl0) * 2) = make_float2(m0, L0);
-        if (v1) *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl1) * 2) = make_float2(m1, L1);
-      }
     }
 
     __syncwarp();
@@ -605,34 +657,33 @@ struct Int4Variant {
   int P;
 };
 
-template <int D, int BS, int MT>
+template <int D, int BS, int NH, int MT>
 static Int4Variant make_int4_variant() {
   Int4Variant v;
-  v.fn = (const void*)decode_int4_kernel<D, BS, MT>;
-  const int stage = Int4Tile<D, BS>::STAGE;
-  v.stages = ring_stages(stage, "PKV_STAGES_INT4");
+  v.fn = (const void*)decode_int4_kernel<D, BS, NH, MT>;
+  v.stages = ring_stages(Int4Tile<D, BS>::STAGE, 16384, "PKV_STAGES_INT4");
   v.smem = int4_smem_bytes<D, BS>(v.stages);
   v.warps = MT;
   v.P = 0;
   return v;
 }
 
-static Int4Variant* lookup_int4(int D, int BS, int MT) {
+static Int4Variant* lookup_int4(int D, int BS, int tiling) {
   static std::mutex mu;
-  static Int4Variant table[2][3][3];
-  static bool ready[2][3][3] = {};
-  const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2), mi = MT == 1 ? 0 : (MT == 2 ? 1 : 2);
+  static Int4Variant table[2][3][4];
+  static bool ready[2][3][4] = {};
+  const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2), ti = tiling;
   std::lock_guard<std::mutex> lock(mu);
-  Int4Variant& v = table[di][bi][mi];
-  if (!ready[di][bi][mi]) {
-#define PKV_V(d, b, m) \
-  if (D == d && BS == b && MT == m) v = make_int4_variant<d, b, m>();
-    PKV_V(64, 16, 1) PKV_V(64, 16, 2) PKV_V(64, 16, 4)
-    PKV_V(64, 32, 1) PKV_V(64, 32, 2) PKV_V(64, 32, 4)
-    PKV_V(64, 64, 1) PKV_V(64, 64, 2) PKV_V(64, 64, 4)
-    PKV_V(128, 16, 1) PKV_V(128, 16, 2) PKV_V(128, 16, 4)
-    PKV_V(128, 32, 1) PKV_V(128, 32, 2) PKV_V(128, 32, 4)
-    PKV_V(128, 64, 1) PKV_V(128, 64, 2) PKV_V(128, 64, 4)
+  Int4Variant& v = table[di][bi][ti];
+  if (!ready[di][bi][ti]) {
+#define PKV_V(d, b)                                               \
+  if (D == d && BS == b) {                                        \
+    if (ti == 0) v = make_int4_variant<d, b, 1, 1>();             \
+    else if (ti == 1) v = make_int4_variant<d, b, 2, 1>();        \
+    else if (ti == 2) v = make_int4_variant<d, b, 2, 2>();        \
+    else v = make_int4_variant<d, b, 2, 4>();                     \
+  }
+    PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
     if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v.smem) != cudaSuccess)
       return nullptr;
@@ -640,13 +691,13 @@ static Int4Variant* lookup_int4(int D, int BS, int MT) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.warps * 32, v.smem) != cudaSuccess || occ < 1)
       return nullptr;
     v.P = device_sm_count() * occ;
-    ready[di][bi][mi] = true;
+    ready[di][bi][ti] = true;
   }
   return &v;
 }
 
 int int4_pieces(int D, int BS, int G) {
-  Int4Variant* v = lookup_int4(D, BS, mt_for_group(G));
+  Int4Variant* v = lookup_int4(D, BS, head_tiling(G));
   return v ? v->P : 0;
 }
 
@@ -731,7 +782,7 @@ extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k
     return PKV_EINVAL;
   if ((long long)max_blocks * block_size > 0x7fffffffLL) return PKV_ERANGE;
   const int G = n_h / n_kv;
-  Int4Variant* vv = lookup_int4(head_dim, block_size, mt_for_group(G));
+  Int4Variant* vv = lookup_int4(head_dim, block_size, head_tiling(G));
   if (!vv) {
     record_cuda_error(cudaGetLastError());
     return PKV_ECUDA;
