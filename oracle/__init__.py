@@ -30,7 +30,7 @@ pages state, brute force on tiny inputs, textbook special cases).  None is
 """
 from .rounding import round_bf16, round_fp16_from_f32
 from .paged_attention import (kv_append, gather_sequence, paged_decode_attention,
-                              attention_weights)
+                              attention_weights, window_start, layer_windows)
 from .kv_sizes import kv_bytes, kv_bytes_gqa, kv_bytes_per_token
 from .int4 import (quantize_group, quantize_groups, pack_codes, unpack_codes, Int4Cache,
                    paged_decode_attention_int4)
@@ -41,5 +41,6 @@ __all__ = [
     "round_bf16", "round_fp16_from_f32", "kv_append", "gather_sequence",
     "paged_decode_attention", "attention_weights", "kv_bytes", "kv_bytes_gqa",
     "kv_bytes_per_token", "quantize_group", "quantize_groups", "pack_codes", "unpack_codes", "Int4Cache",
-    "paged_decode_attention_int4", "rope_shift_k", "rotate", "attention_loops",
+    "paged_decode_attention_int4", "rope_shift_k", "rotate", "attention_loops", "window_start",
+    "layer_windows",
 ]

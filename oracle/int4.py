@@ -168,37 +168,42 @@ class Int4Cache:
             if (tails[i], blk) not in completed:
                 self.k_tail[tails[i], :, row] = k[i]
 
-    def k_rows(self, s, table_row, ctx, g):
-        """Logical K rows 0..ctx-1 of kv group g of batch row s: x^ of full blocks, then the bf16 tail."""
+    def k_rows(self, s, table_row, ctx, g, start=0):
+        """Logical K rows start..ctx-1 of kv group g of batch row s: x^ of full blocks, then the
+        bf16 tail.  Only the blocks holding those rows are read."""
         bs, D = self.bs, self.D
         full = int(ctx) // bs
+        b0 = int(start) // bs
         parts = []
-        for i in range(full):
+        for i in range(b0, full):
             blk = int(table_row[i])
             codes = unpack_codes(self.k_codes[blk, g])
             parts.append(dequantize(codes, self.k_meta[blk, g, 0][None, :], self.k_meta[blk, g, 1][None, :]))
         if int(ctx) > full * bs:
             parts.append(self.k_tail[s, g, : int(ctx) - full * bs])
-        if not parts:
+        if not parts or int(start) >= int(ctx):
             return np.zeros((0, D))
-        return np.concatenate([np.asarray(p, dtype=np.float64) for p in parts], axis=0)
+        rows = np.concatenate([np.asarray(p, dtype=np.float64) for p in parts], axis=0)
+        return rows[int(start) - b0 * bs:]
 
-    def v_rows(self, table_row, ctx, g):
-        """Logical V rows 0..ctx-1 of kv group g: x^ with per-token scale and min."""
+    def v_rows(self, table_row, ctx, g, start=0):
+        """Logical V rows start..ctx-1 of kv group g: x^ with per-token scale and min."""
         bs = self.bs
         nb = -(-int(ctx) // bs)
+        b0 = int(start) // bs
         parts = []
-        for i in range(nb):
+        for i in range(b0, nb):
             blk = int(table_row[i])
             codes = unpack_codes(self.v_codes[blk, g])
             parts.append(dequantize(codes, self.v_meta[blk, g, :, 0][:, None], self.v_meta[blk, g, :, 1][:, None]))
-        if not parts:
+        if not parts or int(start) >= int(ctx):
             return np.zeros((0, self.D))
-        return np.concatenate(parts, axis=0)[: int(ctx)].astype(np.float64)
+        return np.concatenate(parts, axis=0)[int(start) - b0 * bs: int(ctx) - b0 * bs].astype(np.float64)
 
 
-def paged_decode_attention_int4(q, cache: Int4Cache, block_tables, context_lens, scale):
-    """Decode attention over the dequantized INT4 cache (float64 on the x^ values)."""
+def paged_decode_attention_int4(q, cache: Int4Cache, block_tables, context_lens, scale, window=0):
+    """Decode attention over the dequantized INT4 cache (float64 on the x^ values); with
+    window > 0 over the last `window` tokens only (read as for the bf16 cache)."""
     q = np.asarray(q, dtype=np.float64)
     B, n_h, d = q.shape
     n_kv = cache.k_codes.shape[1]
@@ -208,9 +213,10 @@ def paged_decode_attention_int4(q, cache: Int4Cache, block_tables, context_lens,
         L = int(context_lens[s])
         if L <= 0:
             continue
+        t0 = max(0, L - int(window)) if window > 0 else 0
         for g in range(n_kv):
-            K = cache.k_rows(s, block_tables[s], L, g)
-            V = cache.v_rows(block_tables[s], L, g)
+            K = cache.k_rows(s, block_tables[s], L, g, t0)
+            V = cache.v_rows(block_tables[s], L, g, t0)
             for h in range(g * G, (g + 1) * G):
                 logits = scale * (K @ q[s, h])
                 w = np.exp(logits - logits.max())

@@ -18,6 +18,12 @@ Sources:
   "KV 캐시 시스템 (KV Cache System)", section "MQA / GQA": n_h query heads share
   n_kv K/V groups (MHA: n_kv = n_h, MQA: n_kv = 1).  Reading: query head h reads
   kv group h // (n_h / n_kv).
+* "KV 캐시 시스템 (KV Cache System)", sections "제한된 어텐션 윈도우 크기 (Limited
+  Attention Window Size)" and "어텐션 윈도우 크기": a layer may limit its attention
+  window, and blocks that fall out of the window are released for reuse.  Reading:
+  with a window of W tokens the query attends to the last W tokens of its context,
+  [L - W, L), the new token included; W = 0 (or W >= L) is full attention; blocks
+  wholly before the window are never read (their table entries may be stale).
 """
 import numpy as np
 
@@ -40,14 +46,29 @@ def kv_append(k_pool, v_pool, k, v, slot_mapping, block_size):
     return kp, vp
 
 
-def gather_sequence(pool, table_row, ctx, g, block_size):
-    """Logical rows 0..ctx-1 of kv group g of one sequence, as a contiguous [ctx][d] array."""
+def gather_sequence(pool, table_row, ctx, g, block_size, start=0):
+    """Logical rows start..ctx-1 of kv group g of one sequence, as a contiguous array.
+
+    Only the blocks holding those rows are read.
+    """
     d = pool.shape[-1]
-    nb = -(-int(ctx) // block_size)
-    if nb == 0:
+    ctx, start = int(ctx), int(start)
+    if start >= ctx:
         return np.zeros((0, d), dtype=np.float64)
-    tiles = [np.asarray(pool[int(table_row[i]), g], dtype=np.float64) for i in range(nb)]
-    return np.concatenate(tiles, axis=0)[: int(ctx)]
+    b0, b1 = start // block_size, -(-ctx // block_size)
+    tiles = [np.asarray(pool[int(table_row[i]), g], dtype=np.float64) for i in range(b0, b1)]
+    return np.concatenate(tiles, axis=0)[start - b0 * block_size: ctx - b0 * block_size]
+
+
+def window_start(ctx, window):
+    """First attended token of a context of ctx tokens under a window of `window` tokens (0 = none)."""
+    return max(0, int(ctx) - int(window)) if window > 0 else 0
+
+
+def layer_windows(max_attention_window, n_layers):
+    """Per-layer windows from a max_attention_window list, repeated when shorter than the model."""
+    w = list(max_attention_window)
+    return [w[i % len(w)] for i in range(n_layers)]
 
 
 def attention_weights(q_h, K, scale):
@@ -57,11 +78,12 @@ def attention_weights(q_h, K, scale):
     return w / w.sum()
 
 
-def paged_decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale, block_size):
+def paged_decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale, block_size, window=0):
     """out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s, K_s / V_s gathered through the block table.
 
     q: [B][n_h][d]; pools: [num_blocks][n_kv][block_size][d]; returns float64 [B][n_h][d].
-    A sequence with context length 0 gives a zero output.
+    A sequence with context length 0 gives a zero output.  With window > 0, K_s / V_s
+    hold only the last `window` tokens.
     """
     q = np.asarray(q, dtype=np.float64)
     B, n_h, d = q.shape
@@ -72,9 +94,10 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale,
         L = int(context_lens[s])
         if L <= 0:
             continue
+        t0 = window_start(L, window)
         for g in range(n_kv):
-            K = gather_sequence(k_pool, block_tables[s], L, g, block_size)
-            V = gather_sequence(v_pool, block_tables[s], L, g, block_size)
+            K = gather_sequence(k_pool, block_tables[s], L, g, block_size, t0)
+            V = gather_sequence(v_pool, block_tables[s], L, g, block_size, t0)
             for h in range(g * G, (g + 1) * G):
                 out[s, h] = attention_weights(q[s, h], K, scale) @ V
     return out
