@@ -50,14 +50,23 @@ METRIC = "paged GQA decode attn: KV-cache HBM GB/s (% of peak) and sequences/s"
 
 # ---------------------------------------------------------------------------------------------
 # algorithmic bytes
+def attended_blocks(w: workloads.Workload, s: int):
+    """(logical block, attended rows) of sequence s: the blocks from the one its attention
+    window starts in (block 0 without a window), with the rows of each that are attended."""
+    c = int(w.context_lens[s])
+    t0 = max(0, c - w.window) if w.window > 0 else 0
+    out = []
+    for i in range(t0 // w.block_size, -(-c // w.block_size)):
+        lo, hi = max(t0, i * w.block_size), min(c, (i + 1) * w.block_size)
+        out.append((i, hi - lo))
+    return out
+
+
 def kv_token_rows(w: workloads.Workload) -> int:
     """Unique (physical block, row) pairs the step must read (shared prefix blocks once)."""
     need = {}
     for s in range(w.batch):
-        c = int(w.context_lens[s])
-        nb = -(-c // w.block_size)
-        for i in range(nb):
-            rows = min(w.block_size, c - i * w.block_size)
+        for i, rows in attended_blocks(w, s):
             p = int(w.block_tables[s, i])
             need[p] = max(need.get(p, 0), rows)
     return sum(need.values())
@@ -76,8 +85,9 @@ def attention_bytes(w, int4=False) -> int:
         tail_rows = 0
         for s in range(w.batch):
             c = int(w.context_lens[s])
-            for i in range(c // w.block_size):
-                full_blocks[int(w.block_tables[s, i])] = 1
+            for i, _ in attended_blocks(w, s):
+                if (i + 1) * w.block_size <= c:
+                    full_blocks[int(w.block_tables[s, i])] = 1
             tail_rows += c % w.block_size
         kv = (rows * w.n_kv * w.head_dim + rows * w.n_kv * 4 + len(full_blocks) * w.n_kv * w.head_dim * 4
               + tail_rows * w.n_kv * w.head_dim * 2)
@@ -85,7 +95,7 @@ def attention_bytes(w, int4=False) -> int:
         kv = rows * w.n_kv * w.head_dim * 2 * 2
     q = w.batch * w.n_h * w.head_dim * 2
     out = w.batch * w.n_h * w.head_dim * 2
-    tables = sum(-(-int(c) // w.block_size) for c in w.context_lens) * 4
+    tables = sum(len(attended_blocks(w, s)) for s in range(w.batch)) * 4
     return kv + q + out + tables + w.batch * 4
 
 
@@ -233,8 +243,12 @@ class Bf16Step:
 
     def attention(self, x=None):
         x = x or self.inputs
-        self.pkv.paged_decode_attn(x["q"], self.k_pool, self.v_pool, x["bt"], x["ctx"], self.w.scale,
-                                   out=self.out, workspace=self.ws, err=self.err)
+        if self.w.window:
+            self.pkv.paged_decode_attn_window(x["q"], self.k_pool, self.v_pool, x["bt"], x["ctx"], self.w.scale,
+                                              self.w.window, out=self.out, workspace=self.ws, err=self.err)
+        else:
+            self.pkv.paged_decode_attn(x["q"], self.k_pool, self.v_pool, x["bt"], x["ctx"], self.w.scale,
+                                       out=self.out, workspace=self.ws, err=self.err)
 
     def step(self, x=None):
         x = x or self.inputs
@@ -280,8 +294,12 @@ class Int4Step:
 
     def attention(self, x=None):
         x = x or self.inputs
-        self.pkv.paged_decode_attn_int4(x["q"], self.cache, x["bt"], x["ctx"], self.w.scale, out=self.out,
-                                        workspace=self.ws, err=self.err)
+        if self.w.window:
+            self.pkv.paged_decode_attn_int4_window(x["q"], self.cache, x["bt"], x["ctx"], self.w.scale,
+                                                   self.w.window, out=self.out, workspace=self.ws, err=self.err)
+        else:
+            self.pkv.paged_decode_attn_int4(x["q"], self.cache, x["bt"], x["ctx"], self.w.scale, out=self.out,
+                                            workspace=self.ws, err=self.err)
 
     def step(self, x=None):
         x = x or self.inputs
@@ -343,7 +361,8 @@ def cpu_samples(name, seed, n_seqs):
         q = f64(workloads.normal_bf16((1, w.n_h, w.head_dim), 1002 + 4 * i))
         kv = f64(workloads.normal_bf16((2, 1, w.n_kv, w.head_dim), 1003 + 4 * i))
         sub = workloads.Workload(w.name, 1, w.n_h, w.n_kv, w.head_dim, w.block_size,
-                                 w.context_lens[s:s + 1], np.arange(nb, dtype=np.int32)[None, :], nb, w.scale)
+                                 w.context_lens[s:s + 1], np.arange(nb, dtype=np.int32)[None, :], nb, w.scale,
+                                 window=w.window)
         out.append((sub, kb, vb, q, kv[0], kv[1], np.array([(c - 1)], dtype=np.int64)))
     return out
 
@@ -358,7 +377,8 @@ def time_cpu(samples, budget_s):
         sub, kb, vb, q, kn, vn, slot = samples[done % len(samples)]
         t0 = time.perf_counter()
         k2, v2 = oracle.kv_append(kb, vb, kn, vn, slot, sub.block_size)
-        oracle.paged_decode_attention(q, k2, v2, sub.block_tables, sub.context_lens, sub.scale, sub.block_size)
+        oracle.paged_decode_attention(q, k2, v2, sub.block_tables, sub.context_lens, sub.scale, sub.block_size,
+                                      window=sub.window)
         elapsed += time.perf_counter() - t0
         nbytes += attention_bytes(sub) + append_bytes(sub)
         done += 1
@@ -540,7 +560,7 @@ def main():
         by = {}
         kk, ww = max(5, min(K, 30)), max(3, min(W, 5))
         for name in ["llama2_70b_prefix", "mqa_bs16", "mqa_bs32", "mha_bs16", "mha_bs32", "rope_mqa_bs16",
-                     "rope_mha_bs32", "int4_long", "int4_long_bs64"]:
+                     "rope_mha_bs32", "int4_long", "int4_long_bs64", "llama3_8b_window256"]:
             if name == args.workload:
                 continue
             st, sb, ab, ag, am = run_config(name, kk, ww, rank, dev, stream, flush_buf, world)

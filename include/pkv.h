@@ -116,6 +116,25 @@ pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* 
                                  int32_t* err_flag, void* stream);
 
 /*
+ * paged_decode_attn_window — pkv_paged_decode_attn for a layer with a limited
+ * attention window.  "KV 캐시 시스템 (KV Cache System)", sections "제한된 어텐션 윈도우
+ * 크기 (Limited Attention Window Size)" and "어텐션 윈도우 크기" (max_attention_window).
+ *   window        tokens the query attends to: the last `window` tokens of the
+ *                 context, [context_lens[s] - window, context_lens[s]); 0 means the
+ *                 whole context (the call is then pkv_paged_decode_attn).  Negative:
+ *                 PKV_EINVAL.
+ *   Table entries of blocks that end before the window are not read (they may hold
+ *   released or reused block ids).  Every other argument, the workspace size and the
+ *   arithmetic: as pkv_paged_decode_attn.
+ */
+pkv_status pkv_paged_decode_attn_window(const void* q, const void* k_pool, const void* v_pool,
+                                        const int32_t* block_tables, int max_blocks,
+                                        const int32_t* context_lens, float scale, int window,
+                                        int batch, int n_h, int n_kv, int head_dim, int block_size,
+                                        int num_blocks, void* out, int out_dtype, void* workspace,
+                                        size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
  * paged_decode_attn_noalloc — pkv_paged_decode_attn without a caller workspace.
  * The reference pages have no counterpart: this entry point exists for callers that
  * cannot allocate device memory when they decode (an engine that gave all free memory
@@ -192,6 +211,21 @@ pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, con
                                       int batch, int n_h, int n_kv, int head_dim, int block_size,
                                       int num_blocks, void* out, int out_dtype, void* workspace,
                                       size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
+ * paged_decode_attn_int4_window — pkv_paged_decode_attn_int4 over the last `window`
+ * tokens of each context (0: the whole context), with the window read as for
+ * pkv_paged_decode_attn_window: K/V codes, metadata and table entries of blocks that end
+ * before the window are not read.
+ */
+pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uint8_t* k_codes, const void* k_meta,
+                                             const uint8_t* v_codes, const void* v_meta,
+                                             const void* k_tail, const int32_t* block_tables,
+                                             int max_blocks, const int32_t* context_lens, float scale,
+                                             int window, int batch, int n_h, int n_kv, int head_dim,
+                                             int block_size, int num_blocks, void* out, int out_dtype,
+                                             void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                             void* stream);
 
 /*
  * rope_shift_k — re-rotate the keys of reused chunks in place.

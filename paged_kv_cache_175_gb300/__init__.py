@@ -6,9 +6,10 @@ and streams.  There is no CPU fallback: the calls raise if the library is not
 built or a tensor is not on a CUDA device.
 
 Functions (same names as the C entry points without the ``pkv_`` prefix):
-``kv_append``, ``paged_decode_attn``, ``kv_quant_append_int4``,
-``paged_decode_attn_int4``, ``rope_shift_k``, plus ``decode_workspace_bytes`` and
-``alloc_int4_cache``.
+``kv_append``, ``paged_decode_attn``, ``paged_decode_attn_window``,
+``paged_decode_attn_noalloc``, ``kv_quant_append_int4``, ``paged_decode_attn_int4``,
+``paged_decode_attn_int4_window``, ``rope_shift_k``, plus ``decode_workspace_bytes``,
+``alloc_int4_cache`` and the host helper ``layer_windows``.
 """
 from __future__ import annotations
 
@@ -41,6 +42,10 @@ _SIGS = {
     "pkv_rope_shift_k": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_double, _P, _P]),
     "pkv_paged_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
                                            _P, _I, _P, _P]),
+    "pkv_paged_decode_attn_window": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I, _I,
+                                          _P, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pkv_paged_decode_attn_int4_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I,
+                                               _I, _I, _I, _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
 }
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -119,6 +124,29 @@ def _out(q, out, out_dtype):
 def paged_decode_attn(q, k_pool, v_pool, block_tables, context_lens, scale, out=None, out_dtype=torch.bfloat16,
                       workspace=None, err=None, stream=None):
     """Decode attention over a paged bf16 cache; returns out [B][n_h][d]."""
+    return _decode_bf16(q, k_pool, v_pool, block_tables, context_lens, scale, 0, out, out_dtype, workspace, err,
+                        stream)
+
+
+def paged_decode_attn_window(q, k_pool, v_pool, block_tables, context_lens, scale, window, out=None,
+                             out_dtype=torch.bfloat16, workspace=None, err=None, stream=None):
+    """Decode attention over the last `window` tokens of each context (0: all of it)."""
+    return _decode_bf16(q, k_pool, v_pool, block_tables, context_lens, scale, int(window), out, out_dtype,
+                        workspace, err, stream)
+
+
+def layer_windows(max_attention_window, n_layers):
+    """Attention window of each layer from a max_attention_window list: the list is
+    repeated when it is shorter than the model (a layer whose window is at least the
+    longest context attends to all of it)."""
+    w = [int(x) for x in max_attention_window]
+    if not w or any(x <= 0 for x in w):
+        raise ValueError("max_attention_window must be a non-empty list of positive token counts")
+    return [w[i % len(w)] for i in range(n_layers)]
+
+
+def _decode_bf16(q, k_pool, v_pool, block_tables, context_lens, scale, window, out, out_dtype, workspace, err,
+                 stream):
     _cuda(q, k_pool, v_pool, block_tables, context_lens, out, workspace, err)
     assert q.dtype == k_pool.dtype == v_pool.dtype == torch.bfloat16
     assert block_tables.dtype == context_lens.dtype == torch.int32
@@ -129,10 +157,16 @@ def paged_decode_attn(q, k_pool, v_pool, block_tables, context_lens, scale, out=
     need = decode_workspace_bytes(B, n_h, n_kv, d, bs)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    _check("paged_decode_attn", lib().pkv_paged_decode_attn(
-        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-        float(scale), B, n_h, n_kv, d, bs, num_blocks, _ptr(out), od, _ptr(workspace), workspace.numel(),
-        _ptr(err), _stream(stream)))
+    if window == 0:
+        _check("paged_decode_attn", lib().pkv_paged_decode_attn(
+            _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            float(scale), B, n_h, n_kv, d, bs, num_blocks, _ptr(out), od, _ptr(workspace), workspace.numel(),
+            _ptr(err), _stream(stream)))
+    else:
+        _check("paged_decode_attn_window", lib().pkv_paged_decode_attn_window(
+            _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            float(scale), window, B, n_h, n_kv, d, bs, num_blocks, _ptr(out), od, _ptr(workspace),
+            workspace.numel(), _ptr(err), _stream(stream)))
     return out
 
 
@@ -190,6 +224,17 @@ def kv_quant_append_int4(k, v, slot_mapping, tail_seq, cache: Int4CacheTensors, 
 def paged_decode_attn_int4(q, cache: Int4CacheTensors, block_tables, context_lens, scale, out=None,
                            out_dtype=torch.bfloat16, workspace=None, err=None, stream=None):
     """Decode attention over the INT4 cache; the batch index is the tail row."""
+    return _decode_int4(q, cache, block_tables, context_lens, scale, 0, out, out_dtype, workspace, err, stream)
+
+
+def paged_decode_attn_int4_window(q, cache: Int4CacheTensors, block_tables, context_lens, scale, window, out=None,
+                                  out_dtype=torch.bfloat16, workspace=None, err=None, stream=None):
+    """INT4 decode attention over the last `window` tokens of each context (0: all of it)."""
+    return _decode_int4(q, cache, block_tables, context_lens, scale, int(window), out, out_dtype, workspace, err,
+                        stream)
+
+
+def _decode_int4(q, cache, block_tables, context_lens, scale, window, out, out_dtype, workspace, err, stream):
     _cuda(q, block_tables, context_lens, out, workspace, err)
     assert q.dtype == torch.bfloat16
     B, n_h, d = q.shape
@@ -199,10 +244,17 @@ def paged_decode_attn_int4(q, cache: Int4CacheTensors, block_tables, context_len
     need = decode_workspace_bytes(B, n_h, n_kv, d, bs, int4=True)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    _check("paged_decode_attn_int4", lib().pkv_paged_decode_attn_int4(
-        _ptr(q), _ptr(cache.k_codes), _ptr(cache.k_meta), _ptr(cache.v_codes), _ptr(cache.v_meta),
-        _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), B, n_h,
-        n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
+    if window == 0:
+        _check("paged_decode_attn_int4", lib().pkv_paged_decode_attn_int4(
+            _ptr(q), _ptr(cache.k_codes), _ptr(cache.k_meta), _ptr(cache.v_codes), _ptr(cache.v_meta),
+            _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), B,
+            n_h, n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
+    else:
+        _check("paged_decode_attn_int4_window", lib().pkv_paged_decode_attn_int4_window(
+            _ptr(q), _ptr(cache.k_codes), _ptr(cache.k_meta), _ptr(cache.v_codes), _ptr(cache.v_meta),
+            _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale),
+            window, B, n_h, n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err),
+            _stream(stream)))
     return out
 
 

@@ -34,8 +34,9 @@ __host__ __device__ constexpr size_t bf16_smem_bytes(int stages) {
   return 1024 + (size_t)stages * (Bf16Tile<D, BS>::STAGE + 16 + 16);
 }
 
-__device__ __forceinline__ uint32_t mask_pair(uint32_t b, int t, int ntok) {
-  return b & ((t < ntok ? 0x0000ffffu : 0u) | (t + 1 < ntok ? 0xffff0000u : 0u));
+// Keep the halves of a pair of rows (t, t + 1) that lie in [lead, ntok); zero the others.
+__device__ __forceinline__ uint32_t mask_pair(uint32_t b, int t, int lead, int ntok) {
+  return b & ((t < ntok && t >= lead ? 0x0000ffffu : 0u) | (t + 1 < ntok && t + 1 >= lead ? 0xffff0000u : 0u));
 }
 
 template <int D, int BS, int NH, int MT>
@@ -90,12 +91,12 @@ __global__ void __launch_bounds__(MT * 32)
       } else {
         w_seq = cur.s; w_base = cur.blk;
         const int b = w_base + lane;
-        w_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + b) : -1;
+        w_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
       }
       n_seq = cur.s;
       n_base = w_base + 32 < cur.nb ? w_base + 32 : 0;
       const int b = n_base + lane;
-      n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + b) : -1;
+      n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
     }
     const int phys = __shfl_sync(FULL_MASK, w_phys, cur.blk - w_base);
     if (lane == 0) {
@@ -106,14 +107,15 @@ __global__ void __launch_bounds__(MT * 32)
         set_err(a.err, PKV_DEV_TIMEOUT);
         abort_flag = 1;
       }
-      const int ntok = cur.blk == cur.nb - 1 ? cur.ctx - cur.blk * BS : BS;
+      const int ntok = cur.blk == cur.nb - 1 ? cur.ctx - (cur.b0 + cur.blk) * BS : BS;
+      const int lead = cur.blk == 0 ? window_lead(cur.ctx, a.window, BS) : 0;
       int flags = 0;
       if (j == 0 || cur.blk == 0) flags |= F_FIRST;
       if (j == len - 1 || cur.blk == cur.nb - 1) flags |= F_LAST;
       if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
       const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
       if (ok) flags |= F_VALID; else set_err(a.err, PKV_DEV_BAD_BLOCK);
-      meta[slot] = make_int4(cur.s, cur.g, cur.blk, ntok | (flags << 8));
+      meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, lead, flags));
       if (ok && ok_wait) {
         mbar_arrive_expect_tx(&full[slot], T::STAGE);
         uint8_t* st = smem + (size_t)slot * T::STAGE;
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(MT * 32)
     }
     consumed = j + 1;
     const int4 mt = meta[slot];
-    const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = mt.w >> 8;
+    const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;   // first q head of the group
 
     if (flags & F_FIRST) {
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(MT * 32)
             for (int r = 0; r < 2; ++r) {
               const int tok = t * 16 + gid + 8 * r;
               float x = sc[t][nh][2 * r + e] * a.scale_log2;
-              if (tok >= ntok) x = -INFINITY;
+              if (tok >= ntok || tok < lead) x = -INFINITY;
               sc[t][nh][2 * r + e] = x;
               mx = fmaxf(mx, x);
             }
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(MT * 32)
           }
       }
       // ---- O^T += V^T P^T, P as bf16 high + low ----
-      const bool partial = ntok < BS;
+      const bool partial = ntok < BS || lead > 0;
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
         // B fragments of P^T (k = token, n = head): the S^T rows of tokens 0-7 / 8-15 of
@@ -289,10 +291,10 @@ __global__ void __launch_bounds__(MT * 32)
           uint32_t va[4];
           ldsm_x4_t(va[0], va[1], va[2], va[3], addr);
           if (partial) {
-            va[0] = mask_pair(va[0], t0, ntok);
-            va[1] = mask_pair(va[1], t0, ntok);
-            va[2] = mask_pair(va[2], t0 + 8, ntok);
-            va[3] = mask_pair(va[3], t0 + 8, ntok);
+            va[0] = mask_pair(va[0], t0, lead, ntok);
+            va[1] = mask_pair(va[1], t0, lead, ntok);
+            va[2] = mask_pair(va[2], t0 + 8, lead, ntok);
+            va[3] = mask_pair(va[3], t0 + 8, lead, ntok);
           }
 #pragma unroll
           for (int nh = 0; nh < NH; ++nh) {
@@ -445,13 +447,12 @@ extern "C" size_t pkv_decode_workspace_bytes(int batch, int n_h, int n_kv, int h
   return workspace_layout(batch, n_kv, G, head_dim, P).total;
 }
 
-extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
-                                            const int32_t* block_tables, int max_blocks,
-                                            const int32_t* context_lens, float scale, int batch, int n_h,
-                                            int n_kv, int head_dim, int block_size, int num_blocks, void* out,
-                                            int out_dtype, void* workspace, size_t workspace_bytes,
-                                            int32_t* err_flag, void* stream) {
-  if (batch < 0 || !valid_shape(n_h, n_kv, head_dim, block_size) || max_blocks < 0 || num_blocks < 0)
+static pkv_status decode_bf16(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                              int max_blocks, const int32_t* context_lens, float scale, int window, int batch,
+                              int n_h, int n_kv, int head_dim, int block_size, int num_blocks, void* out,
+                              int out_dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                              void* stream) {
+  if (batch < 0 || !valid_shape(n_h, n_kv, head_dim, block_size) || max_blocks < 0 || num_blocks < 0 || window < 0)
     return PKV_EINVAL;
   if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32) return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
@@ -500,6 +501,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
   a.ws_o = reinterpret_cast<float*>(ws + wl.o);
   a.err = err_flag;
   a.stages = v->stages;
+  a.window = window;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = a.inline_plan ? cudaSuccess
@@ -514,6 +516,26 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
     return PKV_ECUDA;
   }
   return PKV_OK;
+}
+
+extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
+                                            const int32_t* block_tables, int max_blocks,
+                                            const int32_t* context_lens, float scale, int batch, int n_h,
+                                            int n_kv, int head_dim, int block_size, int num_blocks, void* out,
+                                            int out_dtype, void* workspace, size_t workspace_bytes,
+                                            int32_t* err_flag, void* stream) {
+  return decode_bf16(q, k_pool, v_pool, block_tables, max_blocks, context_lens, scale, 0, batch, n_h, n_kv, head_dim,
+                     block_size, num_blocks, out, out_dtype, workspace, workspace_bytes, err_flag, stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_attn_window(const void* q, const void* k_pool, const void* v_pool,
+                                                   const int32_t* block_tables, int max_blocks,
+                                                   const int32_t* context_lens, float scale, int window, int batch,
+                                                   int n_h, int n_kv, int head_dim, int block_size, int num_blocks,
+                                                   void* out, int out_dtype, void* workspace,
+                                                   size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  return decode_bf16(q, k_pool, v_pool, block_tables, max_blocks, context_lens, scale, window, batch, n_h, n_kv,
+                     head_dim, block_size, num_blocks, out, out_dtype, workspace, workspace_bytes, err_flag, stream);
 }
 
 // ---------------------------------------------------------------------------------------------

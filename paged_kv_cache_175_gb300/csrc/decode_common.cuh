@@ -37,6 +37,7 @@ struct DecodeArgs {
   // lengths and clamp them to [0, max_ctx] themselves.
   const int32_t* ctx_raw;
   int max_ctx, block_size, inline_plan;
+  int window;                    // attention window in tokens (0: the whole context)
   // INT4 cache (unused by the bf16 kernel)
   const uint8_t* k_codes;
   const uint8_t* v_codes;
@@ -72,6 +73,21 @@ __host__ inline WorkspaceLayout workspace_layout(int B, int n_kv, int G, int D, 
   return w;
 }
 
+// Limited attention window: a sequence of ctx tokens attends to its last `window` tokens,
+// [ctx - window, ctx), when window > 0; its segment holds only the blocks from the one
+// the window starts in, so blocks before the window are never read.
+__host__ __device__ __forceinline__ int window_first_block(int ctx, int window, int bs) {
+  return (window > 0 && ctx > window) ? (ctx - window) / bs : 0;
+}
+// Rows of the window's first block that lie before the window.
+__host__ __device__ __forceinline__ int window_lead(int ctx, int window, int bs) {
+  return (window > 0 && ctx > window) ? (ctx - window) % bs : 0;
+}
+// Blocks a sequence's segment covers.
+__host__ __device__ __forceinline__ int span_blocks(int ctx, int window, int bs) {
+  return (ctx + bs - 1) / bs - window_first_block(ctx, window, bs);
+}
+
 // Piece that holds line position pos (the largest p with floor(p W / P) <= pos).
 __device__ __forceinline__ int piece_of(long long pos, long long W, int P) {
   return (int)(((pos + 1) * (long long)P - 1) / W);
@@ -79,7 +95,8 @@ __device__ __forceinline__ int piece_of(long long pos, long long W, int P) {
 
 // Warp-uniform cursor over the line of positions.
 struct Cursor {
-  int s, g, blk, nb, ctx;
+  int s, g, blk, nb, ctx;        // blk counts from the segment's first block
+  int b0;                        // logical block of the segment's first block (window start)
   long long seg_start;           // line position of block 0 of segment (s, g)
 };
 
@@ -91,6 +108,7 @@ __device__ __forceinline__ void cursor_from_table(Cursor& c, int p, long long ps
   c.blk = e0.z;
   c.nb = e0.w;
   c.ctx = e1.x;
+  c.b0 = window_first_block(c.ctx, a.window, a.block_size);
   c.seg_start = pstart - c.blk;
 }
 
@@ -133,7 +151,7 @@ __device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_la
     if (c < nch) {
       bad |= cv[c] < 0 || cv[c] > a.max_ctx;
       cv[c] = clamp_ctx(cv[c], a.max_ctx);
-      int nb = (cv[c] + a.block_size - 1) / a.block_size;
+      int nb = span_blocks(cv[c], a.window, a.block_size);
 #pragma unroll
       for (int o = 16; o; o >>= 1) nb += __shfl_xor_sync(FULL_MASK, nb, o);
       total += nb;
@@ -150,7 +168,7 @@ __device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_la
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
     if (c >= nch || found) continue;
-    const int nb = (cv[c] + a.block_size - 1) / a.block_size;
+    const int nb = span_blocks(cv[c], a.window, a.block_size);
     int incl = nb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -165,6 +183,7 @@ __device__ __forceinline__ void piece_setup(const DecodeArgs& a, int p, int P_la
       cur.s = c * 32 + src;
       cur.nb = __shfl_sync(FULL_MASK, nb, src);
       cur.ctx = __shfl_sync(FULL_MASK, cv[c], src);
+      cur.b0 = window_first_block(cur.ctx, a.window, a.block_size);
       const long long off = pi.pstart - lo_s;
       cur.g = (int)(off / cur.nb);
       cur.blk = (int)(off % cur.nb);
@@ -188,20 +207,26 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
     do {
       ++c.s;
       c.ctx = clamp_ctx(a.ctx_raw[c.s], a.max_ctx);
-      c.nb = (c.ctx + a.block_size - 1) / a.block_size;
+      c.nb = span_blocks(c.ctx, a.window, a.block_size);
     } while (c.nb == 0 && c.s < a.batch - 1);
-    return;
+  } else {
+    do {
+      ++c.s;
+      c.nb = a.cum[c.s + 1] - a.cum[c.s];
+    } while (c.nb == 0 && c.s < a.batch - 1);
+    c.ctx = a.ctx_eff[c.s];
   }
-  do {
-    ++c.s;
-    c.nb = a.cum[c.s + 1] - a.cum[c.s];
-  } while (c.nb == 0 && c.s < a.batch - 1);
-  c.ctx = a.ctx_eff[c.s];
+  c.b0 = window_first_block(c.ctx, a.window, a.block_size);
 }
 
 // Host launchers (decode_plan.cu).
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,
                         const DecodeArgs& a, int P, cudaStream_t stream);
+// Packing of a tile's row range into the ring's metadata word: rows [lead, ntok) of the
+// block are attended (lead > 0 only in a window's first block), plus the F_ flags.
+__host__ __device__ __forceinline__ int pack_rows(int ntok, int lead, int flags) {
+  return ntok | (flags << 8) | (lead << 16);
+}
 cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream);
 cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void** args);

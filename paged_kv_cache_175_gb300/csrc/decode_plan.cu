@@ -83,7 +83,8 @@ cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cud
 constexpr int kPlanSeqs = 8192;
 
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ ctx, int batch, int max_ctx,
-                                                    int block_size, int n_kv, int P, int32_t* __restrict__ cum,
+                                                    int block_size, int window, int n_kv, int P,
+                                                    int32_t* __restrict__ cum,
                                                     int32_t* __restrict__ ctx_eff, int4* __restrict__ pieces,
                                                     int32_t* err) {
   __shared__ int warp_sums[32];
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         c = c < 0 ? 0 : max_ctx;
       }
       ctx_eff[s] = c;
-      nb = (c + block_size - 1) / block_size;
+      nb = span_blocks(c, window, block_size);
     }
     int x = nb;                                               // inclusive warp scan
 #pragma unroll
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,
                         const DecodeArgs& a, int P, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(context_lens, batch, max_ctx, block_size, a.n_kv, P,
+  plan_kernel<<<1, 1024, 0, stream>>>(context_lens, batch, max_ctx, block_size, a.window, a.n_kv, P,
                                       const_cast<int32_t*>(a.cum), const_cast<int32_t*>(a.ctx_eff),
                                       const_cast<int4*>(a.pieces), a.err);
   return cudaGetLastError();
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
       for (int c = 0; c < MAXC; ++c) {
         if (c >= nch) continue;
         const int sq = c * 32 + lane;
-        const int b = (clamp_ctx(cv[c], a.max_ctx) + a.block_size - 1) / a.block_size;
+        const int b = span_blocks(clamp_ctx(cv[c], a.max_ctx), a.window, a.block_size);
         int mine = sq == s ? b : 0, prev = sq < s ? b : 0, all = b;
 #pragma unroll
         for (int o = 16; o; o >>= 1) {

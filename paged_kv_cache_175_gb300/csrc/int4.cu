@@ -238,8 +238,9 @@ __device__ __forceinline__ uint32_t dq2(uint32_t h1024, uint32_t s2, uint32_t m2
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) { return pack_f16(bf16_lo(w), bf16_hi(w)); }
-__device__ __forceinline__ uint32_t mask_pair_h(uint32_t b, int t, int ntok) {
-  return b & ((t < ntok ? 0x0000ffffu : 0u) | (t + 1 < ntok ? 0xffff0000u : 0u));
+// Keep the halves of a pair of rows (t, t + 1) that lie in [lead, ntok); zero the others.
+__device__ __forceinline__ uint32_t mask_pair_h(uint32_t b, int t, int lead, int ntok) {
+  return b & ((t < ntok && t >= lead ? 0x0000ffffu : 0u) | (t + 1 < ntok && t + 1 >= lead ? 0xffff0000u : 0u));
 }
 
 template <int D, int BS>
@@ -298,12 +299,12 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
       } else {
         w_seq = cur.s; w_base = cur.blk;
         const int b = w_base + lane;
-        w_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + b) : -1;
+        w_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
       }
       n_seq = cur.s;
       n_base = w_base + 32 < cur.nb ? w_base + 32 : 0;
       const int b = n_base + lane;
-      n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + b) : -1;
+      n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
     }
     const int phys = __shfl_sync(FULL_MASK, w_phys, cur.blk - w_base);
     if (lane == 0) {
@@ -314,14 +315,15 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
         set_err(a.err, PKV_DEV_TIMEOUT);
         abort_flag = 1;
       }
-      const int ntok = cur.blk == cur.nb - 1 ? cur.ctx - cur.blk * BS : BS;
+      const int ntok = cur.blk == cur.nb - 1 ? cur.ctx - (cur.b0 + cur.blk) * BS : BS;
+      const int lead = cur.blk == 0 ? window_lead(cur.ctx, a.window, BS) : 0;
       int flags = 0;
       if (j == 0 || cur.blk == 0) flags |= F_FIRST;
       if (j == len - 1 || cur.blk == cur.nb - 1) flags |= F_LAST;
       if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
       const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
       if (ok) flags |= F_VALID; else set_err(a.err, PKV_DEV_BAD_BLOCK);
-      meta[slot] = make_int4(cur.s, cur.g, cur.blk, ntok | (flags << 8));
+      meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, lead, flags));
       const char* tail = reinterpret_cast<const char*>(a.k_tail + ((size_t)cur.s * a.n_kv + cur.g) * BS * D);
       if (ok && ok_wait) {
         uint8_t* st = smem + (size_t)slot * T::STAGE;
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
     }
     consumed = j + 1;
     const int4 mt = meta[slot];
-    const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = mt.w >> 8;
+    const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;
 
     if (flags & F_FIRST) {
@@ -405,7 +407,8 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
 
     if (flags & F_VALID) {
       const uint8_t* st = smem + (size_t)slot * T::STAGE;
-      const bool partial = ntok < BS;
+      const bool partial = ntok < BS;                            // the unfinished block: K from the tail
+      const bool masked = partial || lead > 0;
       // ---- S^T = K^ Q^T (fp16 in, fp32 accumulate; even / odd k-steps in two accumulators) ----
       float sc[TT][NH][4], sx[TT][NH][4];
 #pragma unroll
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
             for (int r = 0; r < 2; ++r) {
               const int tok = t * 16 + gid + 8 * r;
               float x = sc[t][nh][2 * r + e] * a.scale_log2;
-              if (tok >= ntok) x = -INFINITY;
+              if (tok >= ntok || tok < lead) x = -INFINITY;
               sc[t][nh][2 * r + e] = x;
               mx = fmaxf(mx, x);
             }
@@ -552,8 +555,16 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
             bl[nh][r] = movmatrix_t(lo);
           }
         const int t0 = t * 16 + 2 * tig;                         // a0/a1: tokens t0, t0+1; a2/a3: +8
-        const uint32_t sA = prmt(vm[t0], vm[t0 + 1], 0x5410), mA = prmt(vm[t0], vm[t0 + 1], 0x7632);
-        const uint32_t sB = prmt(vm[t0 + 8], vm[t0 + 9], 0x5410), mB = prmt(vm[t0 + 8], vm[t0 + 9], 0x7632);
+        uint32_t sA = prmt(vm[t0], vm[t0 + 1], 0x5410), mA = prmt(vm[t0], vm[t0 + 1], 0x7632);
+        uint32_t sB = prmt(vm[t0 + 8], vm[t0 + 9], 0x5410), mB = prmt(vm[t0 + 8], vm[t0 + 9], 0x7632);
+        if (masked) {
+          // rows outside [lead, ntok) get scale = min = 0, so their V^ is exactly 0 whatever
+          // their codes (rows past ntok were never written)
+          sA = mask_pair_h(sA, t0, lead, ntok);
+          mA = mask_pair_h(mA, t0, lead, ntok);
+          sB = mask_pair_h(sB, t0 + 8, lead, ntok);
+          mB = mask_pair_h(mB, t0 + 8, lead, ntok);
+        }
         const uint8_t* vc = st + T::VC + cv / 2;
 #pragma unroll
         for (int w = 0; w < VW; ++w) {
@@ -570,12 +581,6 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
             va[1] = dq2(lop_nib(pab >> 4), sA, mA);              // row gid+8 (odd nibble)
             va[2] = dq2(lop_nib(pcd), sB, mB);                   // row gid,   tokens t0+8, t0+9
             va[3] = dq2(lop_nib(pcd >> 4), sB, mB);
-            if (partial) {
-              va[0] = mask_pair_h(va[0], t0, ntok);
-              va[1] = mask_pair_h(va[1], t0, ntok);
-              va[2] = mask_pair_h(va[2], t0 + 8, ntok);
-              va[3] = mask_pair_h(va[3], t0 + 8, ntok);
-            }
 #pragma unroll
             for (int nh = 0; nh < NH; ++nh) {
               mma_f16(o[4 * w + k][nh], va, bh[nh][0], bh[nh][1]);
@@ -763,14 +768,12 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
   return PKV_OK;
 }
 
-extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, const void* k_meta,
-                                                 const uint8_t* v_codes, const void* v_meta, const void* k_tail,
-                                                 const int32_t* block_tables, int max_blocks,
-                                                 const int32_t* context_lens, float scale, int batch, int n_h,
-                                                 int n_kv, int head_dim, int block_size, int num_blocks, void* out,
-                                                 int out_dtype, void* workspace, size_t workspace_bytes,
-                                                 int32_t* err_flag, void* stream) {
-  if (batch < 0 || !valid_shape(n_h, n_kv, head_dim, block_size) || max_blocks < 0 || num_blocks < 0)
+static pkv_status decode_int4(const void* q, const uint8_t* k_codes, const void* k_meta, const uint8_t* v_codes,
+                              const void* v_meta, const void* k_tail, const int32_t* block_tables, int max_blocks,
+                              const int32_t* context_lens, float scale, int window, int batch, int n_h, int n_kv,
+                              int head_dim, int block_size, int num_blocks, void* out, int out_dtype, void* workspace,
+                              size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  if (batch < 0 || !valid_shape(n_h, n_kv, head_dim, block_size) || max_blocks < 0 || num_blocks < 0 || window < 0)
     return PKV_EINVAL;
   if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32) return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
@@ -813,6 +816,7 @@ extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k
   a.ws_o = reinterpret_cast<float*>(ws + wl.o);
   a.err = err_flag;
   a.stages = vv->stages;
+  a.window = window;
   a.k_codes = k_codes;
   a.v_codes = v_codes;
   a.k_meta = static_cast<const __half*>(k_meta);
@@ -831,4 +835,29 @@ extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k
     return PKV_ECUDA;
   }
   return PKV_OK;
+}
+
+extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, const void* k_meta,
+                                                 const uint8_t* v_codes, const void* v_meta, const void* k_tail,
+                                                 const int32_t* block_tables, int max_blocks,
+                                                 const int32_t* context_lens, float scale, int batch, int n_h,
+                                                 int n_kv, int head_dim, int block_size, int num_blocks, void* out,
+                                                 int out_dtype, void* workspace, size_t workspace_bytes,
+                                                 int32_t* err_flag, void* stream) {
+  return decode_int4(q, k_codes, k_meta, v_codes, v_meta, k_tail, block_tables, max_blocks, context_lens, scale, 0,
+                     batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace, workspace_bytes,
+                     err_flag, stream);
+}
+
+extern "C" pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uint8_t* k_codes, const void* k_meta,
+                                                        const uint8_t* v_codes, const void* v_meta,
+                                                        const void* k_tail, const int32_t* block_tables,
+                                                        int max_blocks, const int32_t* context_lens, float scale,
+                                                        int window, int batch, int n_h, int n_kv, int head_dim,
+                                                        int block_size, int num_blocks, void* out, int out_dtype,
+                                                        void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                                        void* stream) {
+  return decode_int4(q, k_codes, k_meta, v_codes, v_meta, k_tail, block_tables, max_blocks, context_lens, scale,
+                     window, batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace,
+                     workspace_bytes, err_flag, stream);
 }

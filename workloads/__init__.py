@@ -21,6 +21,9 @@ Workloads (shapes of the decode layers the reference pages talk about):
 * ``int4_long``   32 q / 8 kv heads, head_dim 128, batch 32, ctx ~ U[8192, 32768],
                   K with 4 outlier channels per kv head (std 10), block 16
                   (``int4_long_bs64``: block 64).
+* ``<name>_window<W>``  the named workload for a layer with a limited attention
+                  window of W tokens (e.g. ``llama3_8b_window256``: the 256-token
+                  layers of a max_attention_window = [4096, 256] model).
 """
 from __future__ import annotations
 
@@ -47,6 +50,7 @@ class Workload:
     n_sharers: int = 0
     outlier_channels: np.ndarray | None = None   # int [n_kv][4] (int4 workload only)
     extra: dict = field(default_factory=dict)
+    window: int = 0                   # attention window in tokens (0: whole context)
 
     @property
     def group(self) -> int:
@@ -102,6 +106,11 @@ def make(name: str, seed: int = 0) -> Workload:
     A suffix ``_b<N>`` keeps the first N context lengths of the named workload with a
     pool sized for them (a smaller case of the same shape, e.g. for profiler captures).
     """
+    wbase, _, wv = name.rpartition("_window")
+    if wbase and wv.isdigit():
+        w = make(wbase, seed)
+        w.name, w.window = name, int(wv)
+        return w
     base, _, nb = name.rpartition("_b")
     if base and nb.isdigit() and base in NAMES:
         w = make(base, seed)
