@@ -1,19 +1,21 @@
 // Paged decode attention over a bf16 cache (GQA / MHA / MQA).
 //
 // Persistent grid: CTA p streams piece p of the (sequence, kv head, block) line (see
-// decode_common.cuh).  Warp 0 also acts as the producer: it walks the piece with a
-// cursor, reads block-table entries 32 at a time (and the next 32 ahead), and for each
-// position issues two TMA tensor loads per tile (K and V, 64-channel boxes with the
-// 128-byte swizzle) into a ring of `stages` shared-memory slots guarded by full/empty
-// mbarriers.  Each consumer warp owns 16 query heads of the group (an m16 tile; MT
-// warps cover the group), so one K/V read serves every head of the group.
+// decode_common.cuh).  A producer walks the piece with a cursor, reads block-table
+// entries 32 at a time (and the next 32 ahead), and for each position issues two TMA
+// tensor loads per 64-channel box (K and V, 128-byte swizzle) into a ring of `stages`
+// shared-memory slots guarded by full/empty mbarriers.  The producer is a warp of its
+// own for groups of up to 8 heads and consumer warp 0 otherwise.  Consumer warps split
+// the group's heads (8 or 16 each), so one K/V read serves every head of the group.
 //
-// Per block: S = Q K^T with mma.m16n8k16 (bf16 in, fp32 accumulate; K B-fragments by
-// ldmatrix from the swizzled tile), base-2 online softmax in fp32 with the scale folded
-// in, then O += P V with P split into a bf16 high part and a bf16 low part (two mma per
-// tile) so the only rounding of P is below 2^-16 relative; V B-fragments by
-// ldmatrix.trans.  Segments finished inside the piece are normalised and stored; cut
-// segments store (m, l, O) partials for the reduce kernel.
+// Per block, token-major: S^T = K Q^T with mma.m16n8k16 (the block's tokens on M, heads
+// on N; bf16 in, fp32 accumulate; K A-fragments by ldmatrix from the swizzled tile),
+// base-2 online softmax over tokens in fp32 with the scale folded in, then
+// O^T += V^T P^T with V^T A-fragments by ldmatrix.trans and P^T B-fragments from S^T's
+// by an in-register 8x8 transpose; P is split into a bf16 high part and a bf16 low part
+// (two mma per tile) so the only rounding of P is below 2^-16 relative.  Segments
+// finished inside the piece are normalised and stored; cut segments store (m, l, O)
+// partials for the reduce kernel.
 #include <cmath>
 #include <mutex>
 
@@ -39,8 +41,13 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t b, int t, int lead, int n
   return b & ((t < ntok && t >= lead ? 0x0000ffffu : 0u) | (t + 1 < ntok && t + 1 >= lead ? 0xffff0000u : 0u));
 }
 
-template <int D, int BS, int NH, int MT>
-__global__ void __launch_bounds__(MT * 32)
+// PW: a dedicated producer warp (warp MT) streams the ring ahead of the consumer warps;
+// otherwise consumer warp 0 issues each tile's loads itself after consuming a tile.  The
+// dedicated warp takes the block-table walk, the barrier bookkeeping and the copy issue
+// (about as many cycles per tile as the tile's arithmetic) off the consumers' path; it
+// costs one warp of registers, so it is used where the consumers are light (one warp).
+template <int D, int BS, int NH, int MT, bool PW>
+__global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32, (PW && BS == 16) ? 8 : 0)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const DecodeArgs a) {
   using T = Bf16Tile<D, BS>;
@@ -71,16 +78,17 @@ __global__ void __launch_bounds__(MT * 32)
   grid_dep_wait();                  // plan kernel's cum / ctx_eff are visible after this
   grid_dep_launch();
 
+  const int producer_warp = PW ? MT : 0;
   Cursor cur;
   PieceInfo pi;
-  piece_setup(a, blockIdx.x, gridDim.x, warp == 0, cur, pi);
+  piece_setup(a, blockIdx.x, gridDim.x, warp == producer_warp, cur, pi);
   const int P = pi.P, p = blockIdx.x;
   if (p >= P) return;
   const long long pstart = pi.pstart, pend = pi.pend;
   const int len = (int)(pend - pstart);
   if (len <= 0) return;
 
-  // ---------------- producer state (warp 0, warp-uniform) ----------------
+  // ---------------- producer state (warp-uniform) ----------------
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
 
@@ -145,7 +153,20 @@ __global__ void __launch_bounds__(MT * 32)
   const int gid = lane >> 2;                    // token row / channel row / head column
   const int hw0 = warp * HW;                    // first local head of this warp
 
-  if (warp == 0) {
+  if (PW && warp == MT) {
+    int j = 0;
+    for (; j < len && !abort_flag; ++j) issue(j);
+    if (abort_flag && lane == 0) {
+      // let the copies still in flight land before the CTA exits: wait (bounded) for the
+      // last tile issued on each slot
+      for (int k = 0; k < S && k < j; ++k) {
+        const int last = k + ((j - 1 - k) / S) * S;
+        if (!mbar_wait(&full[k], (last / S) & 1)) break;
+      }
+    }
+    return;
+  }
+  if (!PW && warp == 0) {
     const int pre = len < S ? len : S;
     for (int j = 0; j < pre; ++j) issue(j);
   }
@@ -358,12 +379,12 @@ __global__ void __launch_bounds__(MT * 32)
 
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    if (warp == 0 && j + S < len) issue(j + S);
+    if (!PW && warp == 0 && j + S < len) issue(j + S);
   }
 
   // After a timeout: let this CTA's copies already in flight land before exiting
   // (each wait is bounded, and the drain as a whole gives up at the first failure).
-  if (abort_flag && threadIdx.x == 0) {
+  if (!PW && abort_flag && threadIdx.x == 0) {
     const int issued = len < consumed + S ? len : consumed + S;
     for (int j = consumed; j < issued; ++j)
       if (!mbar_wait(&full[j % S], (j / S) & 1)) break;
@@ -380,14 +401,16 @@ struct Bf16Variant {
   int P;        // persistent CTAs on this device
 };
 
-template <int D, int BS, int NH, int MT>
+template <int D, int BS, int NH, int MT, bool PW>
 static Bf16Variant make_variant() {
   Bf16Variant v;
-  v.fn = (const void*)decode_bf16_kernel<D, BS, NH, MT>;
+  v.fn = (const void*)decode_bf16_kernel<D, BS, NH, MT, PW>;
   v.stage_bytes = Bf16Tile<D, BS>::STAGE;
-  v.stages = ring_stages(v.stage_bytes, 24576, "PKV_STAGES_BF16");
+  // measured best: 16 KB of ring per CTA with the dedicated producer (its consumer keeps
+  // up, and more resident CTAs beat deeper prefetch), 24 KB with the inline one
+  v.stages = ring_stages(v.stage_bytes, PW ? 16384 : 24576, "PKV_STAGES_BF16");
   v.smem = bf16_smem_bytes<D, BS>(v.stages);
-  v.warps = MT;
+  v.warps = MT + (PW ? 1 : 0);
   v.P = 0;
   return v;
 }
@@ -403,10 +426,10 @@ static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   if (!ready[di][bi][ti]) {
 #define PKV_V(d, b)                                               \
   if (D == d && BS == b) {                                        \
-    if (ti == 0) v = make_variant<d, b, 1, 1>();                  \
-    else if (ti == 1) v = make_variant<d, b, 2, 1>();             \
-    else if (ti == 2) v = make_variant<d, b, 2, 2>();             \
-    else v = make_variant<d, b, 2, 4>();                          \
+    if (ti == 0) v = make_variant<d, b, 1, 1, true>();            \
+    else if (ti == 1) v = make_variant<d, b, 2, 1, false>();      \
+    else if (ti == 2) v = make_variant<d, b, 2, 2, false>();      \
+    else v = make_variant<d, b, 2, 4, false>();                   \
   }
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V

@@ -234,10 +234,10 @@ int device_sm_count();
 // Stages of the shared-memory ring for a stage of `stage_bytes`: about `ring_bytes` of
 // ring per CTA, at least 2 and at most 8; the environment variable `env` (an integer
 // 2..16) overrides it for tuning.  A small ring leaves room for more resident CTAs,
-// which these latency-bound kernels need more than deep prefetch (measured: 24 KB for
-// the bf16 cache, 16 KB for INT4).
+// which these kernels need more than deep prefetch (the ring sizes each kernel passes
+// were measured on the benchmark workloads).
 int ring_stages(size_t stage_bytes, size_t ring_bytes, const char* env);
-// Head tiling of a group for the attention kernels: 0 = one warp of 8 heads (G <= 8);
+// Head tiling of a group for the attention kernels: 0 = one consumer warp of 8 heads (G <= 8);
 // 1 / 2 / 3 = 1 / 2 / 4 warps of 16 heads (G <= 16 / 32 / 64).
 inline int head_tiling(int G) { return G <= 8 ? 0 : (G <= 16 ? 1 : (G <= 32 ? 2 : 3)); }
 int bf16_pieces(int D, int BS, int G);
