@@ -48,6 +48,10 @@ FALLBACK_HBM_GBS = 6800.0
 METRIC = "paged GQA decode attn: KV-cache HBM GB/s (% of peak) and sequences/s"
 
 
+# Batches above this many sequences get the library's one-CTA plan kernel before the
+# attention kernel (smaller ones plan inside the attention kernel).
+PLAN_KERNEL_ABOVE = 256
+
 # ---------------------------------------------------------------------------------------------
 # algorithmic bytes
 def attended_blocks(w: workloads.Workload, s: int):
@@ -237,7 +241,8 @@ class Bf16Step:
         nbytes = pkv.decode_workspace_bytes(w.batch, w.n_h, w.n_kv, w.head_dim, w.block_size)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.launches_per_step = 4          # append, plan, attention, split-reduce
+        # append, attention, split-reduce; the library adds a plan kernel above 256 sequences
+        self.launches_per_step = 3 + (w.batch > PLAN_KERNEL_ABOVE)
         self.inputs = {"q": self.q, "kn": self.kn, "vn": self.vn, "slots": self.slots, "bt": self.bt,
                        "ctx": self.ctx}
 
@@ -288,7 +293,8 @@ class Int4Step:
         nbytes = pkv.decode_workspace_bytes(w.batch, w.n_h, w.n_kv, w.head_dim, w.block_size, int4=True)
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.launches_per_step = 5          # quantize, tail update, plan, attention, split-reduce
+        # quantize, tail update, attention, split-reduce (+ plan above 256 sequences)
+        self.launches_per_step = 4 + (w.batch > PLAN_KERNEL_ABOVE)
         self.inputs = {"q": self.q, "kn": self.kn, "vn": self.vn, "slots": self.slots, "tails": self.tails,
                        "bt": self.bt, "ctx": self.ctx}
 
@@ -542,8 +548,8 @@ def main():
         "frac_of_hbm_peak": round(agg["gbs"] / world / peak, 4),
         "e2e": {"value": round(e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e["ms_per_step"], 5)},
-        "roofline": {"bound": "hbm", "kernel": {"Bf16Step": "paged_decode_attn (plan + attention + split-reduce)",
-                                                "Int4Step": "paged_decode_attn_int4 (plan + attention + split-reduce)",
+        "roofline": {"bound": "hbm", "kernel": {"Bf16Step": "paged_decode_attn (attention + split-reduce)",
+                                                "Int4Step": "paged_decode_attn_int4 (attention + split-reduce)",
                                                 "RopeStep": "rope_shift_k"}[type(main_step).__name__],
                      "achieved": round(attn_bytes / (attn_ms / 1e3) / 1e9, 2), "peak": peak,
                      "peak_source": f"{peak_src} (HBM copy, MEASURED_PEAKS.json)" if peak_src == "measured"
