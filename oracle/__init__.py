@@ -12,7 +12,8 @@ bit-exact by construction).
 Sources (web pages; cited by title and section in every function):
 
 * "KV 캐시 시스템 (KV Cache System)" — TensorRT-LLM KV cache wiki page
-  (sections "MQA / GQA", "요청 간 재사용", "제한된 어텐션 윈도우 크기").
+  (sections "MQA / GQA", "요청 간 재사용", "보존 정책", "제한된 어텐션 윈도우
+  크기", "호스트 메모리로의 오프로딩", "어텐션 윈도우 크기").
 * "LLM 서빙과 KV Cache, VLLM" — velog post (sections "KV Cache의 크기 계산
   (naive)", "VLLM", "PagedAttention").
 * "KV Cache는 왜 LLM 서빙의 핵심인가" — iq-blog chapter 2 (sections
@@ -36,11 +37,12 @@ from .int4 import (quantize_group, quantize_groups, pack_codes, unpack_codes, In
                    paged_decode_attention_int4)
 from .rope import rope_shift_k, rotate
 from .brute import attention_loops
+from .block_manager import BlockManager, OutOfBlocks, apply_copies
 
 __all__ = [
     "round_bf16", "round_fp16_from_f32", "kv_append", "gather_sequence",
     "paged_decode_attention", "attention_weights", "kv_bytes", "kv_bytes_gqa",
     "kv_bytes_per_token", "quantize_group", "quantize_groups", "pack_codes", "unpack_codes", "Int4Cache",
     "paged_decode_attention_int4", "rope_shift_k", "rotate", "attention_loops", "window_start",
-    "layer_windows",
+    "layer_windows", "BlockManager", "OutOfBlocks", "apply_copies",
 ]
