@@ -8,8 +8,9 @@ built or a tensor is not on a CUDA device.
 Functions (same names as the C entry points without the ``pkv_`` prefix):
 ``kv_append``, ``paged_decode_attn``, ``paged_decode_attn_window``,
 ``paged_decode_attn_noalloc``, ``kv_quant_append_int4``, ``paged_decode_attn_int4``,
-``paged_decode_attn_int4_window``, ``rope_shift_k``, plus ``decode_workspace_bytes``,
-``alloc_int4_cache`` and the host helper ``layer_windows``.
+``paged_decode_attn_int4_window``, ``rope_shift_k``, ``copy_blocks``, plus
+``decode_workspace_bytes``, ``alloc_int4_cache``, the host helper ``layer_windows``
+and ``BlockManager`` (the ``pkv_bm_*`` calls of include/pkv_bm.h).
 """
 from __future__ import annotations
 
@@ -46,6 +47,18 @@ _SIGS = {
                                           _P, _I, _P, ctypes.c_size_t, _P, _P]),
     "pkv_paged_decode_attn_int4_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I,
                                                _I, _I, _I, _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
+    # block manager (host) and its copy executor
+    "pkv_bm_create": (_P, [_I, _I, _I, _I, _I]),
+    "pkv_bm_destroy": (None, [_P]),
+    "pkv_bm_add_sequence": (_I, [_P, ctypes.c_int64, _P, _I, _P, _I, _P, _I]),
+    "pkv_bm_append_tokens": (_I, [_P, _P, _P, _I, _P, _P]),
+    "pkv_bm_release": (_I, [_P, ctypes.c_int64]),
+    "pkv_bm_slide_window": (_I, [_P, ctypes.c_int64, _I]),
+    "pkv_bm_tables": (_I, [_P, _P, _I, _P, _I, _P]),
+    "pkv_bm_take_copies": (_I, [_P, _P, _I]),
+    "pkv_bm_pending_copies": (_I, [_P]),
+    "pkv_bm_counts": (None, [_P, _P]),
+    "pkv_copy_blocks": (_I, [_P, _I, _P, _P, _I, _P, _P, _I, ctypes.c_size_t, _P]),
 }
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -266,3 +279,110 @@ def rope_shift_k(k_pool, block_ids, deltas, rope_base=10000.0, err=None, stream=
     _check("rope_shift_k", lib().pkv_rope_shift_k(_ptr(k_pool), _ptr(block_ids), _ptr(deltas), block_ids.numel(),
                                                   num_blocks, n_kv, bs, d, float(rope_base), _ptr(err),
                                                   _stream(stream)))
+
+
+# ---------------------------------------------------------------------------------------------
+# Block manager (host, include/pkv_bm.h) and the GPU copies it records.
+COPY_OFFLOAD, COPY_ONLOAD = 0, 1
+BM_COUNTS = ("free", "active", "cached", "host", "reused_tokens", "evictions", "offloads", "onloads", "drops")
+
+
+class _TokenRange(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_int32), ("end", ctypes.c_int32), ("priority", ctypes.c_int32)]
+
+
+class BlockManager:
+    """Physical block ids for a paged cache: cross-request reuse, priority-LRU eviction
+    with retention ranges, host offload.  Host bookkeeping only; see include/pkv_bm.h."""
+
+    def __init__(self, num_blocks, block_size, host_blocks=0, offload_min_priority=35, default_priority=35):
+        import numpy as np
+        self._np = np
+        self.num_blocks, self.block_size, self.host_blocks = num_blocks, block_size, host_blocks
+        self._h = lib().pkv_bm_create(num_blocks, block_size, host_blocks, offload_min_priority, default_priority)
+        if not self._h:
+            raise PkvError("pkv_bm_create: invalid argument")
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h and _lib is not None:
+            _lib.pkv_bm_destroy(h)
+
+    def _a(self, x, dtype):
+        return self._np.ascontiguousarray(x, dtype=dtype)
+
+    def add_sequence(self, seq_id, tokens, ranges=()):
+        """Returns (block table as a list, number of reused prompt tokens)."""
+        np = self._np
+        toks = self._a(tokens, np.int32)
+        rr = (_TokenRange * max(1, len(ranges)))(*[_TokenRange(int(a), int(b), int(c)) for a, b, c in ranges])
+        cap = -(-len(toks) // self.block_size)
+        table = np.empty(max(cap, 1), dtype=np.int32)
+        r = lib().pkv_bm_add_sequence(self._h, int(seq_id), toks.ctypes.data, len(toks), rr, len(ranges),
+                                      table.ctypes.data, cap)
+        if r < 0:
+            _check("bm_add_sequence", r)
+        return table[:cap].tolist(), r
+
+    def append_tokens(self, seq_ids, tokens):
+        """One decode step: the cache slot of each sequence's new token (int64 array)."""
+        np = self._np
+        ids, toks = self._a(seq_ids, np.int64), self._a(tokens, np.int32)
+        slots = np.empty(len(ids), dtype=np.int64)
+        done = ctypes.c_int(0)
+        r = lib().pkv_bm_append_tokens(self._h, ids.ctypes.data, toks.ctypes.data, len(ids), slots.ctypes.data,
+                                       ctypes.byref(done))
+        if r < 0:
+            msg = lib().pkv_status_str(r).decode()
+            raise PkvError(f"bm_append_tokens: {msg} after {done.value} of {len(ids)} sequences")
+        return slots
+
+    def release(self, seq_id):
+        _check("bm_release", lib().pkv_bm_release(self._h, int(seq_id)))
+
+    def slide_window(self, seq_id, window):
+        r = lib().pkv_bm_slide_window(self._h, int(seq_id), int(window))
+        if r < 0:
+            _check("bm_slide_window", r)
+        return r
+
+    def tables(self, seq_ids, max_blocks):
+        """(block tables int32 [n][max_blocks], context lengths int32 [n]) for an attention call."""
+        np = self._np
+        ids = self._a(seq_ids, np.int64)
+        t = np.empty((len(ids), max_blocks), dtype=np.int32)
+        c = np.empty(len(ids), dtype=np.int32)
+        _check("bm_tables", lib().pkv_bm_tables(self._h, ids.ctypes.data, len(ids), t.ctypes.data, max_blocks,
+                                                c.ctypes.data))
+        return t, c
+
+    def take_copies(self):
+        """Copies recorded since the last call: int32 [n][3] rows (kind, src, dst)."""
+        np = self._np
+        n = lib().pkv_bm_pending_copies(self._h)
+        out = np.empty((max(n, 1), 3), dtype=np.int32)
+        r = lib().pkv_bm_take_copies(self._h, out.ctypes.data, n)
+        if r < 0:
+            _check("bm_take_copies", r)
+        return out[:r]
+
+    def counts(self):
+        out = (ctypes.c_int64 * len(BM_COUNTS))()
+        lib().pkv_bm_counts(self._h, out)
+        return dict(zip(BM_COUNTS, list(out)))
+
+
+def copy_blocks(copies, k_pool, v_pool, k_host, v_host, stream=None):
+    """Apply recorded copies (int32 [n][3] rows kind, src, dst) between the device pools and
+    host pools in page-locked memory ([host_blocks][...] tensors of the same block shape)."""
+    import numpy as np
+    _cuda(k_pool, v_pool)
+    for t in (k_host, v_host):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise PkvError("host pools must be contiguous page-locked CPU tensors")
+    assert k_pool.shape[1:] == k_host.shape[1:] and k_pool.dtype == k_host.dtype
+    c = np.ascontiguousarray(copies, dtype=np.int32).reshape(-1, 3)
+    block_bytes = k_pool[0].numel() * k_pool.element_size()
+    _check("copy_blocks", lib().pkv_copy_blocks(c.ctypes.data, len(c), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                                _ptr(k_host), _ptr(v_host), k_host.shape[0], block_bytes,
+                                                _stream(stream)))

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu"]
+SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu", "offload.cu", "block_manager.cpp"]
 HEADERS = ["pkv_device.cuh", "decode_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
@@ -24,7 +24,8 @@ def _nvcc() -> str:
 
 
 def _newest_input() -> float:
-    paths = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "pkv.h"), __file__]
+    paths = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [
+        os.path.join(ROOT, "include", h) for h in ("pkv.h", "pkv_bm.h")] + [__file__]
     return max(os.path.getmtime(p) for p in paths)
 
 
@@ -36,7 +37,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ, src.replace(".cu", ".o"))
+        obj = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -1,5 +1,5 @@
 """The C-ABI library builds here (cross-compiled for sm_103a), loads, and exports every
-entry point include/pkv.h declares.  No compute calls: this machine has no GPU."""
+entry point include/*.h declares.  No compute calls: this machine has no GPU."""
 import os
 import re
 import subprocess
@@ -9,13 +9,16 @@ import pytest
 import paged_kv_cache_175_gb300 as pkv
 from paged_kv_cache_175_gb300 import _build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 
 
 def _declared():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names.update(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -27,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for n in ("pkv_kv_append", "pkv_paged_decode_attn", "pkv_kv_quant_append_int4",
               "pkv_paged_decode_attn_int4", "pkv_rope_shift_k", "pkv_decode_workspace_bytes",
-              "pkv_status_str", "pkv_last_cuda_error"):
+              "pkv_status_str", "pkv_last_cuda_error", "pkv_paged_decode_attn_window",
+              "pkv_paged_decode_attn_int4_window", "pkv_bm_create", "pkv_bm_add_sequence", "pkv_copy_blocks"):
         assert n in names
 
 
