@@ -243,6 +243,7 @@ class Bf16Step:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         # append, attention, split-reduce; the library adds a plan kernel above 256 sequences
         self.launches_per_step = 3 + (w.batch > PLAN_KERNEL_ABOVE)
+        self.attention_launches = self.launches_per_step - 1
         self.inputs = {"q": self.q, "kn": self.kn, "vn": self.vn, "slots": self.slots, "bt": self.bt,
                        "ctx": self.ctx}
 
@@ -295,6 +296,7 @@ class Int4Step:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         # quantize, tail update, attention, split-reduce (+ plan above 256 sequences)
         self.launches_per_step = 4 + (w.batch > PLAN_KERNEL_ABOVE)
+        self.attention_launches = self.launches_per_step - 2
         self.inputs = {"q": self.q, "kn": self.kn, "vn": self.vn, "slots": self.slots, "tails": self.tails,
                        "bt": self.bt, "ctx": self.ctx}
 
@@ -326,6 +328,7 @@ class RopeStep:
         self.deltas = torch.as_tensor(w.extra["rope_deltas"], device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.launches_per_step = 1
+        self.attention_launches = 1
         self.out = None
         self.inputs = {"ids": self.ids, "deltas": self.deltas}
 
@@ -392,6 +395,109 @@ def time_cpu(samples, budget_s):
     info = {"sample": f"{done} sequence decode steps (append + attention, all heads) of the {samples[0][0].name} "
                       f"workload, {elapsed:.1f} s of oracle time", "cores": cores, "kind": "oracle"}
     return nbytes / elapsed / 1e9, done / elapsed, elapsed, info
+
+
+# ---------------------------------------------------------------------------------------------
+def bench_offload(dev, stream, K, W, world, n_blocks=4096):
+    """Offload and onload of n_blocks blocks of the 8B-shaped pool between HBM and
+    page-locked host memory through pkv_copy_blocks, against one contiguous
+    cudaMemcpyAsync of the same bytes each way (the copy engines' ceiling on this node)."""
+    import paged_kv_cache_175_gb300 as pkv
+    w = workloads.make("llama3_8b", 0)
+    shape = (w.num_blocks, w.n_kv, w.block_size, w.head_dim)
+    kp, vp = workloads.pools_bf16(w, 0, dev)
+    hshape = (n_blocks,) + shape[1:]
+    kh = torch.empty(hshape, dtype=torch.bfloat16).pin_memory()
+    vh = torch.empty(hshape, dtype=torch.bfloat16).pin_memory()
+    rng = np.random.default_rng(3)
+    src = rng.permutation(w.num_blocks)[:n_blocks]
+    dst = rng.permutation(w.num_blocks)[:n_blocks]
+    off = np.stack([np.zeros(n_blocks, int), src, np.arange(n_blocks)], 1)
+    on = np.stack([np.ones(n_blocks, int), np.arange(n_blocks), dst], 1)
+    moved = 2 * n_blocks * int(np.prod(shape[1:])) * 2                  # K and V bytes per direction
+    none = lambda: None
+    t_off = reduce_max(statistics.mean(time_steps(lambda: pkv.copy_blocks(off, kp, vp, kh, vh), K, W, none, stream)), world)
+    t_on = reduce_max(statistics.mean(time_steps(lambda: pkv.copy_blocks(on, kp, vp, kh, vh), K, W, none, stream)), world)
+    flat_d = torch.empty(moved // 2, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(moved // 2, dtype=torch.uint8).pin_memory()
+    d2h = lambda: (flat_h.copy_(flat_d, non_blocking=True), flat_h.copy_(flat_d, non_blocking=True))
+    h2d = lambda: (flat_d.copy_(flat_h, non_blocking=True), flat_d.copy_(flat_h, non_blocking=True))
+    t_d2h = reduce_max(statistics.mean(time_steps(d2h, K, W, none, stream)), world)
+    t_h2d = reduce_max(statistics.mean(time_steps(h2d, K, W, none, stream)), world)
+    gb = lambda ms: moved / (ms / 1e3) / 1e9
+    launches = -(-n_blocks // 480)                                       # one wave, 480 copies per launch
+    return ({"blocks": n_blocks, "bytes_per_direction": moved,
+             "offload_gbs": round(gb(t_off), 2), "onload_gbs": round(gb(t_on), 2),
+             "memcpy_d2h_gbs": round(gb(t_d2h), 2), "memcpy_h2d_gbs": round(gb(t_h2d), 2),
+             "offload_frac_of_memcpy": round(t_d2h / t_off, 4), "onload_frac_of_memcpy": round(t_h2d / t_on, 4),
+             "steps": K}, 2 * launches * K)
+
+
+def block_manager_trace(w, seed, decode_steps):
+    """Prompts of the 70B-prefix workload (the sharers' first 2048 tokens identical), each
+    then decoding `decode_steps` tokens: (prompts, decode token matrix)."""
+    rng = np.random.default_rng(seed)
+    prefix = rng.integers(0, 32000, size=w.shared_prefix_blocks * w.block_size)
+    prompts = []
+    for s in range(w.batch):
+        n = int(w.context_lens[s]) - decode_steps
+        own = rng.integers(0, 32000, size=n)
+        if s < w.n_sharers:
+            own[:len(prefix)] = prefix
+        prompts.append(own.astype(np.int32))
+    return prompts, rng.integers(0, 32000, size=(decode_steps, w.batch)).astype(np.int32)
+
+
+def run_block_manager(bm, prompts, decode, add, append, release):
+    """Admit every prompt, run the decode steps, release all, admit them again (prefix
+    reuse); seconds of each phase."""
+    t0 = time.perf_counter()
+    for s, p in enumerate(prompts):
+        add(bm, s, p)
+    t1 = time.perf_counter()
+    ids = np.arange(len(prompts), dtype=np.int64)
+    for row in decode:
+        append(bm, ids, row)
+    t2 = time.perf_counter()
+    for s in range(len(prompts)):
+        release(bm, s)
+    for s, p in enumerate(prompts):
+        add(bm, len(prompts) + s, p)
+    t3 = time.perf_counter()
+    return t1 - t0, t2 - t1, t3 - t2
+
+
+def bench_block_manager(rank, decode_steps=16):
+    """Host cost of the native block manager on a serving trace shaped like the 70B-prefix
+    workload, with the oracle's restatement timed on a bounded sample of it."""
+    import paged_kv_cache_175_gb300 as pkv
+    w = workloads.make("llama2_70b_prefix", rank)
+    prompts, decode = block_manager_trace(w, rank, decode_steps)
+    need = sum(-(-int(c) // w.block_size) for c in w.context_lens)
+    N = int(need * 1.2)
+    for rep in range(2):                              # the first pass warms caches and allocators
+        nat = pkv.BlockManager(N, w.block_size, host_blocks=N // 4)
+        ta, td, tr = run_block_manager(nat, prompts, decode, lambda b, s, p: b.add_sequence(s, p),
+                                       lambda b, i, r: b.append_tokens(i, r), lambda b, s: b.release(s))
+    reused = nat.counts()["reused_tokens"]
+    tokens = int(sum(len(p) for p in prompts))
+    out = {"requests": w.batch, "prompt_tokens": tokens, "decode_steps": decode_steps, "pool_blocks": N,
+           "admit_tokens_per_s": round(tokens / ta, 1), "decode_step_us": round(td / decode_steps * 1e6, 2),
+           "decode_appends_per_s": round(w.batch * decode_steps / td, 1),
+           "readmit_tokens_per_s": round(tokens / tr, 1), "reused_tokens": reused}
+    # the oracle (linear scans) on the first 16 requests and 8 decode steps, smaller pool
+    import oracle
+    sub_p, sub_d = prompts[:16], decode[:8, :16]
+    need_s = sum(-(-(len(p) + 8) // w.block_size) for p in sub_p)
+    ref = oracle.BlockManager(int(need_s * 1.2), w.block_size, host_blocks=need_s // 4)
+    ra, rd, rr = run_block_manager(ref, sub_p, sub_d, lambda b, s, p: b.add_sequence(s, p),
+                                   lambda b, i, r: [b.append_token(int(s), int(t)) for s, t in zip(i, r)],
+                                   lambda b, s: b.release(s))
+    st = int(sum(len(p) for p in sub_p))
+    out["cpu_baseline"] = {"kind": "oracle", "sample": "first 16 requests, 8 decode steps",
+                           "admit_tokens_per_s": round(st / ra, 1),
+                           "decode_appends_per_s": round(16 * 8 / rd, 1)}
+    return out
 
 
 # ---------------------------------------------------------------------------------------------
@@ -557,7 +663,8 @@ def main():
                      "unit": "GB/s", "frac": round(attn_bytes / (attn_ms / 1e3) / 1e9 / peak, 4),
                      "traffic": recorded_traffic(args.workload),
                      "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 5)},
-        "gpu_launches": main_step.launches_per_step * K,
+        # the timed loops: steps, attention alone, end to end
+        "gpu_launches": main_step.launches_per_step * 2 * K + main_step.attention_launches * K,
         "clocks": clocks,
     }
 
@@ -575,9 +682,13 @@ def main():
                         "bytes_per_step": sb, "attn_gbs": round(ab / (am / 1e3) / 1e9, 2),
                         "attn_frac": round(ab / (am / 1e3) / 1e9 / peak, 4), "attn_ms": round(am, 5),
                         "steps": kk}
-            line["gpu_launches"] += st.launches_per_step * kk
+            line["gpu_launches"] += (st.launches_per_step + st.attention_launches) * kk
             del st
             torch.cuda.empty_cache()
+        off, n_launch = bench_offload(dev, stream, kk, ww, world)
+        by["offload_llama3_8b"] = off
+        line["gpu_launches"] += n_launch
+        by["block_manager_llama2_70b_prefix"] = bench_block_manager(rank)
         line["by_config"] = by
 
     # ---- oracle on the host cores (rank 0, one GPU only) ----
