@@ -22,7 +22,8 @@ Sources (web pages; cited by title and section in every function):
   with the quantization equation).
 * "Research Paper Review : CACHE BLEND, Fast Large Language Model Serving for
   RAG with Cached Knowledge Fusion" — tistory review (section "Background",
-  full KV reuse with RoPE re-rotation).
+  full KV reuse with RoPE re-rotation; sections "Methods" and "System Design", KV
+  deviation, token selection and the recompute ratio).
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` (closed forms printed on the pages, invariants the
@@ -38,11 +39,12 @@ from .int4 import (quantize_group, quantize_groups, pack_codes, unpack_codes, In
 from .rope import rope_shift_k, rotate
 from .brute import attention_loops
 from .block_manager import BlockManager, OutOfBlocks, apply_copies
+from . import cacheblend
 
 __all__ = [
     "round_bf16", "round_fp16_from_f32", "kv_append", "gather_sequence",
     "paged_decode_attention", "attention_weights", "kv_bytes", "kv_bytes_gqa",
     "kv_bytes_per_token", "quantize_group", "quantize_groups", "pack_codes", "unpack_codes", "Int4Cache",
     "paged_decode_attention_int4", "rope_shift_k", "rotate", "attention_loops", "window_start",
-    "layer_windows", "BlockManager", "OutOfBlocks", "apply_copies",
+    "layer_windows", "BlockManager", "OutOfBlocks", "apply_copies", "cacheblend",
 ]
