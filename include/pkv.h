@@ -243,6 +243,57 @@ pkv_status pkv_rope_shift_k(void* k_pool, const int32_t* block_ids, const int32_
                             int n_blocks, int num_blocks, int n_kv, int block_size, int head_dim,
                             double rope_base, int32_t* err_flag, void* stream);
 
+/*
+ * CacheBlend's model-free steps ("Research Paper Review : CACHE BLEND ...", sections
+ * "Methods" and "System Design"): the KV deviation of candidate tokens, the selection of
+ * the tokens with the largest deviation under the recompute ratio, and the fuse of their
+ * recomputed K/V into the cache.  Recomputing K/V needs the model and is the caller's.
+ */
+
+/*
+ * kv_deviation — dev[i] = L2 distance between the cached K and V of the token at
+ * slots[i] and its recomputed rows k_new[i], v_new[i], over all kv heads and channels of
+ * K and V together (fp32 accumulation of the squared bf16 differences, then sqrt).
+ *   k_pool,v_pool bf16 [num_blocks][n_kv][block_size][head_dim]
+ *   slots         int64 [n]
+ *   k_new,v_new   bf16 [n][n_kv][head_dim]
+ *   dev           fp32 [n] (device)
+ * A slot outside the pool sets PKV_DEV_BAD_SLOT and gives dev 0.
+ */
+pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, const int64_t* slots, const void* k_new,
+                            const void* v_new, int n, int num_blocks, int block_size, int n_kv, int head_dim,
+                            float* dev, int32_t* err_flag, void* stream);
+
+/*
+ * select_top — for each segment s = [seg_offsets[s], seg_offsets[s+1]) of dev, the
+ * counts[s] elements with the largest values (equal values: lowest index first), written
+ * as ascending global indices to out, segment after segment (segment s starts at the sum
+ * of the earlier segments' counts).  counts are clamped to [0, segment length].  Values
+ * are compared in float32 (NaN above +inf, -0 below +0).
+ *   dev fp32 [seg_offsets[n_seg]], seg_offsets int32 [n_seg + 1] (non-decreasing),
+ *   counts int32 [n_seg], out int32 [sum of counts]; all device memory.
+ */
+pkv_status pkv_select_top(const float* dev, const int32_t* seg_offsets, const int32_t* counts, int n_seg,
+                          int32_t* out, void* stream);
+
+/*
+ * kv_fuse — write the recomputed rows of the selected tokens into the cache:
+ * pools[slots[j]] = k_new[rows[j]], v_new[rows[j]] for j < n_sel.
+ *   k_new,v_new bf16 [n_rows][n_kv][head_dim]; rows int32 [n_sel]; slots int64 [n_sel].
+ * A slot outside the pool or a row outside [0, n_rows) sets PKV_DEV_BAD_SLOT and is skipped.
+ * Slots must be distinct.
+ */
+pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, int n_rows, const int32_t* rows, const int64_t* slots,
+                       int n_sel, void* k_pool, void* v_pool, int num_blocks, int block_size, int n_kv,
+                       int head_dim, int32_t* err_flag, void* stream);
+
+/* The recompute ratio max(15%, load_time / full_recompute_time), at most 1: the ratio at
+ * which recomputing the selected tokens takes as long as loading the layer's KV
+ * ("System Design"), recompute time taken as proportional to the tokens recomputed. */
+double pkv_recompute_ratio(double load_time, double full_recompute_time);
+/* Tokens selected out of n at a ratio: ceil(ratio * n), within [0, n]. */
+int pkv_select_count(double ratio, int n);
+
 #ifdef __cplusplus
 }
 #endif

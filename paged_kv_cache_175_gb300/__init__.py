@@ -8,7 +8,8 @@ built or a tensor is not on a CUDA device.
 Functions (same names as the C entry points without the ``pkv_`` prefix):
 ``kv_append``, ``paged_decode_attn``, ``paged_decode_attn_window``,
 ``paged_decode_attn_noalloc``, ``kv_quant_append_int4``, ``paged_decode_attn_int4``,
-``paged_decode_attn_int4_window``, ``rope_shift_k``, ``copy_blocks``, plus
+``paged_decode_attn_int4_window``, ``rope_shift_k``, ``copy_blocks``, ``kv_deviation``,
+``select_top``, ``kv_fuse``, ``recompute_ratio``, ``select_count``, plus
 ``decode_workspace_bytes``, ``alloc_int4_cache``, the host helper ``layer_windows``
 and ``BlockManager`` (the ``pkv_bm_*`` calls of include/pkv_bm.h).
 """
@@ -59,6 +60,12 @@ _SIGS = {
     "pkv_bm_pending_copies": (_I, [_P]),
     "pkv_bm_counts": (None, [_P, _P]),
     "pkv_copy_blocks": (_I, [_P, _I, _P, _P, _I, _P, _P, _I, ctypes.c_size_t, _P]),
+    # CacheBlend's model-free steps
+    "pkv_kv_deviation": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "pkv_select_top": (_I, [_P, _P, _P, _I, _P, _P]),
+    "pkv_kv_fuse": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "pkv_recompute_ratio": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
+    "pkv_select_count": (_I, [ctypes.c_double, _I]),
 }
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -386,3 +393,55 @@ def copy_blocks(copies, k_pool, v_pool, k_host, v_host, stream=None):
     _check("copy_blocks", lib().pkv_copy_blocks(c.ctypes.data, len(c), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
                                                 _ptr(k_host), _ptr(v_host), k_host.shape[0], block_bytes,
                                                 _stream(stream)))
+
+
+# ---------------------------------------------------------------------------------------------
+# CacheBlend's model-free steps (pkv.h): KV deviation, top-ratio selection, fuse.
+def kv_deviation(k_pool, v_pool, slots, k_new, v_new, err=None, stream=None):
+    """Per-token L2 distance between the cached K/V at slots and the recomputed rows (fp32 [n])."""
+    _cuda(k_pool, v_pool, slots, k_new, v_new, err)
+    assert k_pool.dtype == v_pool.dtype == k_new.dtype == v_new.dtype == torch.bfloat16
+    assert slots.dtype == torch.int64
+    num_blocks, n_kv, bs, d = k_pool.shape
+    n = slots.numel()
+    assert k_new.shape == v_new.shape == (n, n_kv, d)
+    dev = torch.empty(n, dtype=torch.float32, device=k_pool.device)
+    _check("kv_deviation", lib().pkv_kv_deviation(_ptr(k_pool), _ptr(v_pool), _ptr(slots), _ptr(k_new), _ptr(v_new),
+                                                  n, num_blocks, bs, n_kv, d, _ptr(dev), _ptr(err), _stream(stream)))
+    return dev
+
+
+def select_top(dev, seg_offsets, counts, stream=None):
+    """Per segment, the counts[s] largest deviations as ascending global indices (int32).
+    seg_offsets / counts: host sequences (they size the output)."""
+    import numpy as np
+    _cuda(dev)
+    assert dev.dtype == torch.float32
+    offs = np.ascontiguousarray(seg_offsets, dtype=np.int32)
+    cnt = np.ascontiguousarray(counts, dtype=np.int32)
+    assert len(offs) == len(cnt) + 1
+    total = int(np.minimum(np.maximum(cnt, 0), np.maximum(np.diff(offs), 0)).sum())
+    out = torch.empty(max(total, 1), dtype=torch.int32, device=dev.device)
+    o_d = torch.as_tensor(offs, device=dev.device)
+    c_d = torch.as_tensor(cnt, device=dev.device)
+    _check("select_top", lib().pkv_select_top(_ptr(dev), _ptr(o_d), _ptr(c_d), len(cnt), _ptr(out),
+                                              _stream(stream)))
+    return out[:total]
+
+
+def kv_fuse(k_new, v_new, rows, slots, k_pool, v_pool, err=None, stream=None):
+    """pools[slots[j]] = k_new / v_new[rows[j]]: the recomputed rows of the selected tokens."""
+    _cuda(k_new, v_new, rows, slots, k_pool, v_pool, err)
+    assert rows.dtype == torch.int32 and slots.dtype == torch.int64 and rows.numel() == slots.numel()
+    num_blocks, n_kv, bs, d = k_pool.shape
+    _check("kv_fuse", lib().pkv_kv_fuse(_ptr(k_new), _ptr(v_new), k_new.shape[0], _ptr(rows), _ptr(slots),
+                                        rows.numel(), _ptr(k_pool), _ptr(v_pool), num_blocks, bs, n_kv, d, _ptr(err),
+                                        _stream(stream)))
+
+
+def recompute_ratio(load_time, full_recompute_time):
+    return lib().pkv_recompute_ratio(float(load_time), float(full_recompute_time))
+
+
+def select_count(ratio, n):
+    return lib().pkv_select_count(float(ratio), int(n))

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu", "offload.cu", "block_manager.cpp"]
+SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu", "offload.cu", "cacheblend.cu", "block_manager.cpp"]
 HEADERS = ["pkv_device.cuh", "decode_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]

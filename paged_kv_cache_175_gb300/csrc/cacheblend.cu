@@ -1,0 +1,292 @@
+// CacheBlend's model-free steps on the paged cache ("Research Paper Review : CACHE BLEND
+// ...", sections "Methods" and "System Design"): the KV deviation of each candidate token
+// between its reused (precomputed) K/V in the pool and its recomputed K/V, the selection
+// of the tokens with the largest deviation, and the fuse that writes the recomputed rows
+// of the selected tokens into the cache.
+#include <cmath>
+
+#include "../../include/pkv.h"
+#include "decode_common.cuh"
+
+namespace pkv {
+
+// ---- deviation: one warp per token, 16-byte vectors, every load of a pass in flight --------
+constexpr int kDevThreads = 256;
+
+__global__ void __launch_bounds__(kDevThreads)
+    kv_deviation_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
+                        const int64_t* __restrict__ slots, const uint4* __restrict__ k_new,
+                        const uint4* __restrict__ v_new, long long n, int n_kv, int block_size, int vec_per_row,
+                        long long n_slots, float* __restrict__ dev, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (kDevThreads / 32);
+  const int vec_per_tok = n_kv * vec_per_row;
+  for (long long t = blockIdx.x * (long long)(kDevThreads / 32) + (threadIdx.x >> 5); t < n; t += warps) {
+    const long long slot = slots[t];
+    if (slot < 0 || slot >= n_slots) {
+      if (lane == 0) {
+        set_err(err, PKV_DEV_BAD_SLOT);
+        dev[t] = 0.f;
+      }
+      continue;
+    }
+    const long long blk = slot / block_size, row = slot - blk * block_size;
+    const uint4* kn = k_new + t * vec_per_tok;
+    const uint4* vn = v_new + t * vec_per_tok;
+    float acc = 0.f;
+    for (int base = 0; base < vec_per_tok; base += 64) {
+      uint4 a[2], b[2], c[2], d[2];
+      bool ok[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = base + u * 32 + lane;
+        ok[u] = i < vec_per_tok;
+        if (ok[u]) {
+          const int g = i / vec_per_row, w = i - g * vec_per_row;
+          const size_t src = (((size_t)blk * n_kv + g) * block_size + row) * vec_per_row + w;
+          a[u] = __ldg(k_pool + src);
+          b[u] = __ldg(v_pool + src);
+          c[u] = __ldg(kn + i);
+          d[u] = __ldg(vn + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (!ok[u]) continue;
+        const uint32_t* pa = reinterpret_cast<const uint32_t*>(&a[u]);
+        const uint32_t* pb = reinterpret_cast<const uint32_t*>(&b[u]);
+        const uint32_t* pc = reinterpret_cast<const uint32_t*>(&c[u]);
+        const uint32_t* pd = reinterpret_cast<const uint32_t*>(&d[u]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float k0 = bf16_lo(pa[j]) - bf16_lo(pc[j]), k1 = bf16_hi(pa[j]) - bf16_hi(pc[j]);
+          const float v0 = bf16_lo(pb[j]) - bf16_lo(pd[j]), v1 = bf16_hi(pb[j]) - bf16_hi(pd[j]);
+          acc = fmaf(k0, k0, acc);
+          acc = fmaf(k1, k1, acc);
+          acc = fmaf(v0, v0, acc);
+          acc = fmaf(v1, v1, acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
+    if (lane == 0) dev[t] = sqrtf(acc);
+  }
+}
+
+// ---- selection: one CTA per segment, radix select of the k-th largest key ------------------
+// Key of element i of a segment: the order-preserving 32-bit image of its float value in
+// the high half, the complement of i in the low half, so keys are distinct and a larger
+// key means a larger value or, for equal values, a smaller index.
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ uint32_t float_order(float x) {
+  const uint32_t b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ unsigned long long sel_key(const float* dev, int i) {
+  return ((unsigned long long)float_order(dev[i]) << 32) | (uint32_t)~(uint32_t)i;
+}
+
+// Exclusive scan of one int per thread over the CTA; returns this thread's prefix and
+// writes the total to *total (kSelThreads threads).
+__device__ __forceinline__ int cta_exclusive_scan(int x, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - w;                                   // exclusive warp offsets
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + incl - x;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    select_top_kernel(const float* __restrict__ dev, const int32_t* __restrict__ seg_offsets,
+                      const int32_t* __restrict__ counts, int n_seg, int32_t* __restrict__ out) {
+  __shared__ int hist[256];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  __shared__ unsigned long long prefix_sh;
+  __shared__ int remain_sh;
+  const int s = blockIdx.x;
+  const int lo = seg_offsets[s], hi = seg_offsets[s + 1];
+  const int n = hi > lo ? hi - lo : 0;
+  int k = counts[s];
+  k = k < 0 ? 0 : (k > n ? n : k);
+  // output base: the counts of the segments before this one (each clamped the same way)
+  int base = 0;
+  for (int j = threadIdx.x; j < s; j += kSelThreads) {
+    const int nj = seg_offsets[j + 1] - seg_offsets[j];
+    const int kj = counts[j];
+    base += kj < 0 ? 0 : (kj > (nj > 0 ? nj : 0) ? (nj > 0 ? nj : 0) : kj);
+  }
+  base = cta_exclusive_scan(base, warp_tot, &total);
+  base = total;
+  if (k == 0) return;
+  const float* d = dev + lo;
+  unsigned long long thresh = 0;                               // keys >= thresh are selected
+  if (k < n) {
+    // most significant byte first: find the byte of the k-th largest key, pass by pass
+    unsigned long long prefix = 0;
+    int remain = k;
+    for (int pass = 0; pass < 8; ++pass) {
+      const int shift = 56 - 8 * pass;
+      const unsigned long long hmask = pass == 0 ? 0ull : (~0ull << (shift + 8));
+      for (int j = threadIdx.x; j < 256; j += kSelThreads) hist[j] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += kSelThreads) {
+        const unsigned long long key = sel_key(d, i);
+        if ((key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int acc = 0, b = 255;
+        for (; b > 0; --b) {
+          if (acc + hist[b] >= remain) break;
+          acc += hist[b];
+        }
+        remain_sh = remain - acc;
+        prefix_sh = prefix | ((unsigned long long)b << shift);
+      }
+      __syncthreads();
+      prefix = prefix_sh;
+      remain = remain_sh;
+      __syncthreads();
+    }
+    thresh = prefix;                                           // the k-th largest key itself
+  }
+  // compaction in index order
+  int written = 0;
+  for (int c0 = 0; c0 < n; c0 += kSelThreads) {
+    const int i = c0 + threadIdx.x;
+    const int f = (i < n && (k == n || sel_key(d, i) >= thresh)) ? 1 : 0;
+    const int pos = cta_exclusive_scan(f, warp_tot, &total);
+    if (f) out[base + written + pos] = lo + i;
+    written += total;
+    __syncthreads();
+  }
+}
+
+// ---- fuse: recomputed rows of the selected tokens into the pools ----------------------------
+__global__ void __launch_bounds__(256) kv_fuse_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                                      const int32_t* __restrict__ rows,
+                                                      const int64_t* __restrict__ slots, long long total,
+                                                      int vec_per_row, int n_kv, int block_size, long long n_slots,
+                                                      long long n_rows, uint4* __restrict__ k_pool,
+                                                      uint4* __restrict__ v_pool, int32_t* err) {
+  const int vec_per_tok = vec_per_row * n_kv;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long j = idx / vec_per_tok;
+    const int e = (int)(idx - j * vec_per_tok);
+    const int g = e / vec_per_row, vec = e - g * vec_per_row;
+    const long long slot = slots[j];
+    const long long r = rows[j];
+    if (slot < 0 || slot >= n_slots || r < 0 || r >= n_rows) {
+      if (e == 0) set_err(err, PKV_DEV_BAD_SLOT);
+      continue;
+    }
+    const long long blk = slot / block_size, off = slot - blk * block_size;
+    const size_t dst = (((size_t)blk * n_kv + g) * block_size + off) * vec_per_row + vec;
+    k_pool[dst] = k_new[r * vec_per_tok + e];
+    v_pool[dst] = v_new[r * vec_per_tok + e];
+  }
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, const int64_t* slots,
+                                       const void* k_new, const void* v_new, int n, int num_blocks, int block_size,
+                                       int n_kv, int head_dim, float* dev, int32_t* err_flag, void* stream) {
+  if (n < 0 || num_blocks < 0 || block_size < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8) return PKV_EINVAL;
+  if (n == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !slots || !k_new || !v_new || !dev) return PKV_EINVAL;
+  if (!al16(k_pool) || !al16(v_pool) || !al16(k_new) || !al16(v_new)) return PKV_EINVAL;
+  const int vpr = head_dim / 8;
+  const int warps_per_cta = kDevThreads / 32;
+  const long long want = ((long long)n + warps_per_cta - 1) / warps_per_cta;
+  const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
+  kv_deviation_kernel<<<grid, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), slots, static_cast<const uint4*>(k_new),
+      static_cast<const uint4*>(v_new), n, n_kv, block_size, vpr, (long long)num_blocks * block_size, dev,
+      err_flag);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return PKV_ECUDA;
+  }
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_select_top(const float* dev, const int32_t* seg_offsets, const int32_t* counts, int n_seg,
+                                     int32_t* out, void* stream) {
+  if (n_seg < 0) return PKV_EINVAL;
+  if (n_seg == 0) return PKV_OK;
+  if (!dev || !seg_offsets || !counts || !out) return PKV_EINVAL;
+  select_top_kernel<<<n_seg, kSelThreads, 0, static_cast<cudaStream_t>(stream)>>>(dev, seg_offsets, counts, n_seg,
+                                                                                  out);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return PKV_ECUDA;
+  }
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, int n_rows, const int32_t* rows,
+                                  const int64_t* slots, int n_sel, void* k_pool, void* v_pool, int num_blocks,
+                                  int block_size, int n_kv, int head_dim, int32_t* err_flag, void* stream) {
+  if (n_sel < 0 || n_rows < 0 || num_blocks < 0 || block_size < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8)
+    return PKV_EINVAL;
+  if (n_sel == 0) return PKV_OK;
+  if (!k_new || !v_new || !rows || !slots || !k_pool || !v_pool) return PKV_EINVAL;
+  if (!al16(k_new) || !al16(v_new) || !al16(k_pool) || !al16(v_pool)) return PKV_EINVAL;
+  const int vpr = head_dim / 8;
+  const long long total = (long long)n_sel * n_kv * vpr;
+  const long long want = (total + 255) / 256;
+  const int grid = (int)(want < 32LL * device_sm_count() ? want : 32LL * device_sm_count());
+  kv_fuse_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), rows, slots, total, vpr, n_kv, block_size,
+      (long long)num_blocks * block_size, n_rows, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+      err_flag);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return PKV_ECUDA;
+  }
+  return PKV_OK;
+}
+
+extern "C" double pkv_recompute_ratio(double load_time, double full_recompute_time) {
+  double r = full_recompute_time > 0.0 ? load_time / full_recompute_time : 1.0;
+  if (!(r >= 0.15)) r = 0.15;                                  // also catches NaN
+  return r > 1.0 ? 1.0 : r;
+}
+
+extern "C" int pkv_select_count(double ratio, int n) {
+  if (n <= 0 || !(ratio > 0.0)) return 0;
+  const double x = ratio * (double)n - 1e-12;
+  const int k = (int)std::ceil(x);
+  return k < 0 ? 0 : (k > n ? n : k);
+}
