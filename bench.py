@@ -345,11 +345,65 @@ class RopeStep:
         return b, b
 
 
+class BlendStep:
+    """One layer of CacheBlend's model-free steps on the 64 reused 512-token chunks of a
+    workload: KV deviation of every chunk token against its recomputed K/V (synthetic:
+    the cached rows plus noise of a per-token scale), the 15% of each chunk with the
+    largest deviation selected, their recomputed rows fused into the cache."""
+
+    def __init__(self, name, seed, dev):
+        import paged_kv_cache_175_gb300 as pkv
+        self.pkv = pkv
+        self.w = w = workloads.make(name, seed)
+        bs = w.block_size
+        self.k_pool, self.v_pool = workloads.pools_bf16(w, seed, dev)
+        blocks = w.extra["rope_block_ids"].astype(np.int64)
+        slots = (blocks[:, None] * bs + np.arange(bs)[None, :]).reshape(-1)
+        self.n = n = len(slots)
+        self.chunk = 512
+        self.slots = torch.as_tensor(slots, device=dev)
+        g = torch.Generator(device=dev).manual_seed(seed + 17)
+        blk, row = self.slots // bs, self.slots % bs
+        scale = torch.rand(n, 1, 1, generator=g, device=dev) ** 3
+        shape = (n, w.n_kv, w.head_dim)
+        self.kn = (self.k_pool[blk, :, row].float() + scale * torch.randn(*shape, generator=g, device=dev)).to(torch.bfloat16)
+        self.vn = (self.v_pool[blk, :, row].float() + scale * torch.randn(*shape, generator=g, device=dev)).to(torch.bfloat16)
+        n_seg = n // self.chunk
+        self.k_sel = pkv.select_count(0.15, self.chunk)
+        self.offs = torch.arange(0, n + 1, self.chunk, dtype=torch.int32, device=dev)
+        self.counts = torch.full((n_seg,), self.k_sel, dtype=torch.int32, device=dev)
+        self.dev_buf = torch.empty(n, dtype=torch.float32, device=dev)
+        self.sel = torch.empty(n_seg * self.k_sel, dtype=torch.int32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out = None
+        self.launches_per_step = 3                 # deviation, selection, fuse
+        self.attention_launches = 1                # deviation alone
+        self.inputs = {}
+
+    def attention(self, x=None):
+        self.pkv.kv_deviation(self.k_pool, self.v_pool, self.slots, self.kn, self.vn, out=self.dev_buf, err=self.err)
+
+    def step(self, x=None):
+        self.attention()
+        self.pkv.select_top(self.dev_buf, self.offs, self.counts, out=self.sel)
+        self.pkv.kv_fuse(self.kn, self.vn, self.slots, self.sel, self.k_pool, self.v_pool, err=self.err)
+
+    def bytes(self):
+        w = self.w
+        row = w.n_kv * w.head_dim * 2
+        dev_b = 4 * self.n * row + self.n * 8 + self.n * 4          # pool and new rows, slots, dev out
+        k = self.sel.numel()
+        step_b = dev_b + self.n * 4 + k * 4 + k * (8 + 4 * row)      # dev in; ids; slots, new rows in, pool rows out
+        return step_b, dev_b
+
+
 def make_step(name, seed, dev):
     if name.startswith("int4"):
         return Int4Step(name, seed, dev)
     if name.startswith("rope_"):
         return RopeStep(name[5:], seed, dev)
+    if name.startswith("blend_"):
+        return BlendStep(name[6:], seed, dev)
     return Bf16Step(name, seed, dev)
 
 
@@ -646,7 +700,8 @@ def main():
                                f"{w.block_size}, batch {w.batch}, ctx mean {float(np.mean(w.context_lens)):.0f}",
                    "step": {"Bf16Step": "kv_append + paged_decode_attn",
                             "Int4Step": "kv_quant_append_int4 + paged_decode_attn_int4",
-                            "RopeStep": "rope_shift_k"}[type(main_step).__name__],
+                            "RopeStep": "rope_shift_k",
+                            "BlendStep": "kv_deviation + select_top + kv_fuse"}[type(main_step).__name__],
                    "parallelism": f"replicas x{world}",
                    "l2": l2_note,
                    "algorithmic_bytes_per_step": step_bytes},
@@ -656,7 +711,8 @@ def main():
                 "ms_per_step": round(e2e["ms_per_step"], 5)},
         "roofline": {"bound": "hbm", "kernel": {"Bf16Step": "paged_decode_attn (attention + split-reduce)",
                                                 "Int4Step": "paged_decode_attn_int4 (attention + split-reduce)",
-                                                "RopeStep": "rope_shift_k"}[type(main_step).__name__],
+                                                "RopeStep": "rope_shift_k",
+                                                "BlendStep": "kv_deviation"}[type(main_step).__name__],
                      "achieved": round(attn_bytes / (attn_ms / 1e3) / 1e9, 2), "peak": peak,
                      "peak_source": f"{peak_src} (HBM copy, MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
@@ -673,7 +729,8 @@ def main():
         by = {}
         kk, ww = max(5, min(K, 30)), max(3, min(W, 5))
         for name in ["llama2_70b_prefix", "mqa_bs16", "mqa_bs32", "mha_bs16", "mha_bs32", "rope_mqa_bs16",
-                     "rope_mha_bs32", "int4_long", "int4_long_bs64", "llama3_8b_window256"]:
+                     "rope_mha_bs32", "int4_long", "int4_long_bs64", "llama3_8b_window256", "blend_mqa_bs16",
+                     "blend_mha_bs32"]:
             if name == args.workload:
                 continue
             st, sb, ab, ag, am = run_config(name, kk, ww, rank, dev, stream, flush_buf, world)

@@ -278,14 +278,16 @@ pkv_status pkv_select_top(const float* dev, const int32_t* seg_offsets, const in
 
 /*
  * kv_fuse — write the recomputed rows of the selected tokens into the cache:
- * pools[slots[j]] = k_new[rows[j]], v_new[rows[j]] for j < n_sel.
- *   k_new,v_new bf16 [n_rows][n_kv][head_dim]; rows int32 [n_sel]; slots int64 [n_sel].
- * A slot outside the pool or a row outside [0, n_rows) sets PKV_DEV_BAD_SLOT and is skipped.
- * Slots must be distinct.
+ * pools[row_slots[rows[j]]] = k_new[rows[j]], v_new[rows[j]] for j < n_sel (rows as
+ * pkv_select_top returns them, indexing the candidate rows of k_new / v_new).
+ *   k_new,v_new bf16 [n_rows][n_kv][head_dim]; row_slots int64 [n_rows] (the cache slot of
+ *   each candidate row); rows int32 [n_sel].
+ * A row outside [0, n_rows) or a slot outside the pool sets PKV_DEV_BAD_SLOT and is
+ * skipped.  The selected rows' slots must be distinct.
  */
-pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, int n_rows, const int32_t* rows, const int64_t* slots,
-                       int n_sel, void* k_pool, void* v_pool, int num_blocks, int block_size, int n_kv,
-                       int head_dim, int32_t* err_flag, void* stream);
+pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, const int64_t* row_slots, int n_rows,
+                       const int32_t* rows, int n_sel, void* k_pool, void* v_pool, int num_blocks, int block_size,
+                       int n_kv, int head_dim, int32_t* err_flag, void* stream);
 
 /* The recompute ratio max(15%, load_time / full_recompute_time), at most 1: the ratio at
  * which recomputing the selected tokens takes as long as loading the layer's KV

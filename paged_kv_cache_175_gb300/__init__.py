@@ -63,7 +63,7 @@ _SIGS = {
     # CacheBlend's model-free steps
     "pkv_kv_deviation": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "pkv_select_top": (_I, [_P, _P, _P, _I, _P, _P]),
-    "pkv_kv_fuse": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "pkv_kv_fuse": (_I, [_P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
     "pkv_recompute_ratio": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
     "pkv_select_count": (_I, [ctypes.c_double, _I]),
 }
@@ -397,44 +397,49 @@ def copy_blocks(copies, k_pool, v_pool, k_host, v_host, stream=None):
 
 # ---------------------------------------------------------------------------------------------
 # CacheBlend's model-free steps (pkv.h): KV deviation, top-ratio selection, fuse.
-def kv_deviation(k_pool, v_pool, slots, k_new, v_new, err=None, stream=None):
+def kv_deviation(k_pool, v_pool, slots, k_new, v_new, out=None, err=None, stream=None):
     """Per-token L2 distance between the cached K/V at slots and the recomputed rows (fp32 [n])."""
-    _cuda(k_pool, v_pool, slots, k_new, v_new, err)
+    _cuda(k_pool, v_pool, slots, k_new, v_new, out, err)
     assert k_pool.dtype == v_pool.dtype == k_new.dtype == v_new.dtype == torch.bfloat16
     assert slots.dtype == torch.int64
     num_blocks, n_kv, bs, d = k_pool.shape
     n = slots.numel()
     assert k_new.shape == v_new.shape == (n, n_kv, d)
-    dev = torch.empty(n, dtype=torch.float32, device=k_pool.device)
+    dev = torch.empty(n, dtype=torch.float32, device=k_pool.device) if out is None else out
+    assert dev.dtype == torch.float32 and dev.numel() == n
     _check("kv_deviation", lib().pkv_kv_deviation(_ptr(k_pool), _ptr(v_pool), _ptr(slots), _ptr(k_new), _ptr(v_new),
                                                   n, num_blocks, bs, n_kv, d, _ptr(dev), _ptr(err), _stream(stream)))
     return dev
 
 
-def select_top(dev, seg_offsets, counts, stream=None):
+def select_top(dev, seg_offsets, counts, out=None, stream=None):
     """Per segment, the counts[s] largest deviations as ascending global indices (int32).
-    seg_offsets / counts: host sequences (they size the output)."""
+    seg_offsets / counts: host sequences (they size the output), or device int32 tensors
+    together with a device `out` of the right size (no host work, e.g. inside a graph)."""
     import numpy as np
-    _cuda(dev)
+    _cuda(dev, out)
     assert dev.dtype == torch.float32
-    offs = np.ascontiguousarray(seg_offsets, dtype=np.int32)
-    cnt = np.ascontiguousarray(counts, dtype=np.int32)
-    assert len(offs) == len(cnt) + 1
-    total = int(np.minimum(np.maximum(cnt, 0), np.maximum(np.diff(offs), 0)).sum())
-    out = torch.empty(max(total, 1), dtype=torch.int32, device=dev.device)
-    o_d = torch.as_tensor(offs, device=dev.device)
-    c_d = torch.as_tensor(cnt, device=dev.device)
-    _check("select_top", lib().pkv_select_top(_ptr(dev), _ptr(o_d), _ptr(c_d), len(cnt), _ptr(out),
+    if out is None:
+        offs = np.ascontiguousarray(seg_offsets, dtype=np.int32)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        assert len(offs) == len(cnt) + 1
+        total = int(np.minimum(np.maximum(cnt, 0), np.maximum(np.diff(offs), 0)).sum())
+        out = torch.empty(max(total, 1), dtype=torch.int32, device=dev.device)[:total]
+        seg_offsets = torch.as_tensor(offs, device=dev.device)
+        counts = torch.as_tensor(cnt, device=dev.device)
+    _cuda(seg_offsets, counts)
+    assert seg_offsets.dtype == counts.dtype == out.dtype == torch.int32
+    _check("select_top", lib().pkv_select_top(_ptr(dev), _ptr(seg_offsets), _ptr(counts), counts.numel(), _ptr(out),
                                               _stream(stream)))
-    return out[:total]
+    return out
 
 
-def kv_fuse(k_new, v_new, rows, slots, k_pool, v_pool, err=None, stream=None):
-    """pools[slots[j]] = k_new / v_new[rows[j]]: the recomputed rows of the selected tokens."""
-    _cuda(k_new, v_new, rows, slots, k_pool, v_pool, err)
-    assert rows.dtype == torch.int32 and slots.dtype == torch.int64 and rows.numel() == slots.numel()
+def kv_fuse(k_new, v_new, row_slots, rows, k_pool, v_pool, err=None, stream=None):
+    """pools[row_slots[rows[j]]] = k_new / v_new[rows[j]]: the recomputed rows of the selected tokens."""
+    _cuda(k_new, v_new, rows, row_slots, k_pool, v_pool, err)
+    assert rows.dtype == torch.int32 and row_slots.dtype == torch.int64 and row_slots.numel() == k_new.shape[0]
     num_blocks, n_kv, bs, d = k_pool.shape
-    _check("kv_fuse", lib().pkv_kv_fuse(_ptr(k_new), _ptr(v_new), k_new.shape[0], _ptr(rows), _ptr(slots),
+    _check("kv_fuse", lib().pkv_kv_fuse(_ptr(k_new), _ptr(v_new), _ptr(row_slots), k_new.shape[0], _ptr(rows),
                                         rows.numel(), _ptr(k_pool), _ptr(v_pool), num_blocks, bs, n_kv, d, _ptr(err),
                                         _stream(stream)))
 

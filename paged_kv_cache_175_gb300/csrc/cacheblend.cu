@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ int warp_tot[32];
   __shared__ int total;
   __shared__ unsigned long long prefix_sh;
-  __shared__ int remain_sh;
+  __shared__ int remain_sh, done_sh;
   const int s = blockIdx.x;
   const int lo = seg_offsets[s], hi = seg_offsets[s + 1];
   const int n = hi > lo ? hi - lo : 0;
@@ -143,7 +143,9 @@ __global__ void __launch_bounds__(kSelThreads)
   const float* d = dev + lo;
   unsigned long long thresh = 0;                               // keys >= thresh are selected
   if (k < n) {
-    // most significant byte first: find the byte of the k-th largest key, pass by pass
+    // most significant byte first: find the byte of the k-th largest key, pass by pass;
+    // stop early once the bin holding it is taken whole (then every key at or above the
+    // prefix is selected)
     unsigned long long prefix = 0;
     int remain = k;
     for (int pass = 0; pass < 8; ++pass) {
@@ -156,21 +158,47 @@ __global__ void __launch_bounds__(kSelThreads)
         if ((key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int acc = 0, b = 255;
-        for (; b > 0; --b) {
-          if (acc + hist[b] >= remain) break;
-          acc += hist[b];
+      if (threadIdx.x < 32) {
+        // lane l holds bins 255-8l down to 248-8l; counts from the top bin downwards
+        const int lane = threadIdx.x;
+        int c[8], tot = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          c[u] = hist[255 - 8 * lane - u];
+          tot += c[u];
         }
-        remain_sh = remain - acc;
-        prefix_sh = prefix | ((unsigned long long)b << shift);
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int above = incl - tot;                             // keys in higher bins
+        // the lane whose bins take the cumulative count to `remain` holds the k-th key
+        // (bin 0 of lane 31 catches whatever is left)
+        if (above < remain && (incl >= remain || lane == 31)) {
+          int b = 255 - 8 * lane;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (above + c[u] >= remain || (lane == 31 && u == 7)) {
+              b = 255 - 8 * lane - u;
+              remain_sh = remain - above;
+              done_sh = (c[u] == remain - above) ? 1 : 0;
+              prefix_sh = prefix | ((unsigned long long)b << shift);
+              break;
+            }
+            above += c[u];
+          }
+        }
       }
       __syncthreads();
       prefix = prefix_sh;
       remain = remain_sh;
+      const int done = done_sh;
       __syncthreads();
+      if (done) break;
     }
-    thresh = prefix;                                           // the k-th largest key itself
+    thresh = prefix;                       // the k-th largest key, or the prefix of its whole bin
   }
   // compaction in index order
   int written = 0;
@@ -186,8 +214,8 @@ __global__ void __launch_bounds__(kSelThreads)
 
 // ---- fuse: recomputed rows of the selected tokens into the pools ----------------------------
 __global__ void __launch_bounds__(256) kv_fuse_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-                                                      const int32_t* __restrict__ rows,
-                                                      const int64_t* __restrict__ slots, long long total,
+                                                      const int64_t* __restrict__ row_slots,
+                                                      const int32_t* __restrict__ rows, long long total,
                                                       int vec_per_row, int n_kv, int block_size, long long n_slots,
                                                       long long n_rows, uint4* __restrict__ k_pool,
                                                       uint4* __restrict__ v_pool, int32_t* err) {
@@ -197,9 +225,9 @@ __global__ void __launch_bounds__(256) kv_fuse_kernel(const uint4* __restrict__ 
     const long long j = idx / vec_per_tok;
     const int e = (int)(idx - j * vec_per_tok);
     const int g = e / vec_per_row, vec = e - g * vec_per_row;
-    const long long slot = slots[j];
     const long long r = rows[j];
-    if (slot < 0 || slot >= n_slots || r < 0 || r >= n_rows) {
+    const long long slot = (r >= 0 && r < n_rows) ? row_slots[r] : -1;
+    if (slot < 0 || slot >= n_slots) {
       if (e == 0) set_err(err, PKV_DEV_BAD_SLOT);
       continue;
     }
@@ -254,22 +282,22 @@ extern "C" pkv_status pkv_select_top(const float* dev, const int32_t* seg_offset
   return PKV_OK;
 }
 
-extern "C" pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, int n_rows, const int32_t* rows,
-                                  const int64_t* slots, int n_sel, void* k_pool, void* v_pool, int num_blocks,
+extern "C" pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, const int64_t* row_slots, int n_rows,
+                                  const int32_t* rows, int n_sel, void* k_pool, void* v_pool, int num_blocks,
                                   int block_size, int n_kv, int head_dim, int32_t* err_flag, void* stream) {
   if (n_sel < 0 || n_rows < 0 || num_blocks < 0 || block_size < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8)
     return PKV_EINVAL;
   if (n_sel == 0) return PKV_OK;
-  if (!k_new || !v_new || !rows || !slots || !k_pool || !v_pool) return PKV_EINVAL;
+  if (!k_new || !v_new || !rows || !row_slots || !k_pool || !v_pool) return PKV_EINVAL;
   if (!al16(k_new) || !al16(v_new) || !al16(k_pool) || !al16(v_pool)) return PKV_EINVAL;
   const int vpr = head_dim / 8;
   const long long total = (long long)n_sel * n_kv * vpr;
   const long long want = (total + 255) / 256;
   const int grid = (int)(want < 32LL * device_sm_count() ? want : 32LL * device_sm_count());
   kv_fuse_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), rows, slots, total, vpr, n_kv, block_size,
-      (long long)num_blocks * block_size, n_rows, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
-      err_flag);
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), row_slots, rows, total, vpr, n_kv,
+      block_size, (long long)num_blocks * block_size, n_rows, static_cast<uint4*>(k_pool),
+      static_cast<uint4*>(v_pool), err_flag);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);

@@ -76,15 +76,15 @@ def test_fuse_is_exact():
     kn = torch.randn(200, 8, 128).to(torch.bfloat16)
     vn = torch.randn(200, 8, 128).to(torch.bfloat16)
     rows = rng.choice(200, size=60, replace=False).astype(np.int32)
-    slots = rng.permutation(40 * 16)[:60].astype(np.int64)
+    row_slots = rng.permutation(40 * 16)[:200].astype(np.int64)          # a distinct slot per candidate row
     kd, vd = kp.to(DEV), vp.to(DEV)
     err = err_flag()
-    pkv.kv_fuse(kn.to(DEV), vn.to(DEV), torch.as_tensor(rows, device=DEV), torch.as_tensor(slots, device=DEV), kd, vd,
-                err=err)
+    pkv.kv_fuse(kn.to(DEV), vn.to(DEV), torch.as_tensor(row_slots, device=DEV), torch.as_tensor(rows, device=DEV),
+                kd, vd, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     bits = lambda t: t.cpu().view(torch.int16).numpy()
-    rk, rv = cb.fuse(bits(kp), bits(vp), bits(kn), bits(vn), rows, slots, 16)
+    rk, rv = cb.fuse(bits(kp), bits(vp), bits(kn), bits(vn), rows, row_slots[rows], 16)
     assert np.array_equal(bits(kd), rk) and np.array_equal(bits(vd), rv)
 
 
@@ -113,7 +113,7 @@ def test_full_size_layer_step(name):
     k = pkv.select_count(0.15, 512)
     sel = pkv.select_top(dev, offs, [k] * 64)
     k_before, v_before = kp.clone(), vp.clone()
-    pkv.kv_fuse(kn, vn, sel, s_d[sel.long()], kp, vp, err=err)
+    pkv.kv_fuse(kn, vn, s_d, sel, kp, vp, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and sel.numel() == 64 * k
     # deviation: sampled tokens against fp64
