@@ -53,7 +53,7 @@ struct WorkspaceLayout {
 // Pieces actually used for a line of W positions when P CTAs are launched: at least
 // kMinPiece positions per piece, so a small batch is not cut into one-tile parts whose
 // merge would cost more than streaming them.
-constexpr int kMinPiece = 16;
+constexpr int kMinPiece = 8;
 __host__ __device__ inline int effective_pieces(long long W, int P) {
   const long long q = (W + kMinPiece - 1) / kMinPiece;
   return (int)(q < 1 ? 1 : (q < P ? q : P));

@@ -18,7 +18,7 @@ def bounds(p, W, P):
     return W * p // P, W * (p + 1) // P
 
 
-def effective_pieces(W, P, min_piece=16):
+def effective_pieces(W, P, min_piece=8):
     return max(1, min(P, -(-W // min_piece)))
 
 
@@ -45,7 +45,7 @@ def test_segment_walk_and_part_indices(seed):
         return
     P = int(rng.choice([3, 50, 608, W, 2 * W + 1]))
     if seed % 2:
-        P = effective_pieces(W, P)          # the kernels cap the grid at ceil(W / 16) pieces
+        P = effective_pieces(W, P)          # the kernels cap the grid at ceil(W / 8) pieces
         assert all(bounds(p, W, P)[1] > bounds(p, W, P)[0] for p in range(P))   # no empty piece
     parts = set()
     for s in range(B):
