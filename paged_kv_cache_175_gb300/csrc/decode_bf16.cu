@@ -47,7 +47,8 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t b, int t, int lead, int n
 // (about as many cycles per tile as the tile's arithmetic) off the consumers' path; it
 // costs one warp of registers, so it is used where the consumers are light (one warp).
 template <int D, int BS, int NH, int MT, bool PW>
-__global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32, (PW && BS == 16) ? 65536 / ((MT + 1) * 32 * 128) : 0)
+__global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
+                                  (PW && BS == 16) ? (NH == 1 ? 65536 / ((MT + 1) * 32 * 128) : 4) : 0)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const DecodeArgs a) {
   using T = Bf16Tile<D, BS>;
@@ -428,7 +429,7 @@ static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   if (D == d && BS == b) {                                        \
     if (ti == 0) v = make_variant<d, b, 1, 1, true>();            \
     else if (ti == 1) v = make_variant<d, b, 1, 2, true>();       \
-    else if (ti == 2) v = make_variant<d, b, 1, 4, true>();       \
+    else if (ti == 2) v = make_variant<d, b, 2, 2, true>();       \
     else v = make_variant<d, b, 2, 4, false>();                   \
   }
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
