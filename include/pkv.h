@@ -289,6 +289,16 @@ pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, const int64_t* row_
                        const int32_t* rows, int n_sel, void* k_pool, void* v_pool, int num_blocks, int block_size,
                        int n_kv, int head_dim, int32_t* err_flag, void* stream);
 
+/*
+ * selftest_wait — exercise the bounded wait that guards every shared-memory ring (the
+ * pages have no counterpart: this checks the failure detection of this library).  One
+ * thread initialises an mbarrier for one arrival, arrives on it (arrive != 0) or not, and
+ * waits for the phase at most limit_us microseconds (1 .. 2 000 000).  A wait that runs out
+ * sets PKV_DEV_TIMEOUT in *err_flag (device int32) and the kernel returns normally; the
+ * context stays usable.  PKV_EINVAL for a limit out of range or a NULL flag.
+ */
+pkv_status pkv_selftest_wait(int arrive, int limit_us, int32_t* err_flag, void* stream);
+
 /* The recompute ratio max(15%, load_time / full_recompute_time), at most 1: the ratio at
  * which recomputing the selected tokens takes as long as loading the layer's KV
  * ("System Design"), recompute time taken as proportional to the tokens recomputed. */

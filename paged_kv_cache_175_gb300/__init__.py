@@ -66,6 +66,7 @@ _SIGS = {
     "pkv_kv_fuse": (_I, [_P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P]),
     "pkv_recompute_ratio": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
     "pkv_select_count": (_I, [ctypes.c_double, _I]),
+    "pkv_selftest_wait": (_I, [_I, _I, _P, _P]),
 }
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -450,3 +451,9 @@ def recompute_ratio(load_time, full_recompute_time):
 
 def select_count(ratio, n):
     return lib().pkv_select_count(float(ratio), int(n))
+
+
+def selftest_wait(arrive, limit_us, err, stream=None):
+    """Run the bounded-wait self-test; err (device int32) gets DEV_TIMEOUT if the wait ran out."""
+    _cuda(err)
+    _check("selftest_wait", lib().pkv_selftest_wait(1 if arrive else 0, int(limit_us), _ptr(err), _stream(stream)))

@@ -304,6 +304,17 @@ cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t
   return launch_pdl(fn, grid, block, 0, stream, kargs);
 }
 
+// Self-test of the bounded wait every ring uses: one thread initialises an mbarrier for
+// one arrival, arrives on it or not, and waits for the phase with a short limit.
+__global__ void wait_selftest_kernel(int arrive, unsigned long long limit_ns, int32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (arrive) mbar_arrive(&bar);
+  if (!mbar_wait(&bar, 0, limit_ns)) set_err(err, PKV_DEV_TIMEOUT);
+}
+
 }  // namespace pkv
 
 extern "C" const char* pkv_status_str(int status) {
@@ -318,3 +329,16 @@ extern "C" const char* pkv_status_str(int status) {
 }
 
 extern "C" int pkv_last_cuda_error(void) { return pkv::g_last_cuda_error; }
+
+extern "C" pkv_status pkv_selftest_wait(int arrive, int limit_us, int32_t* err_flag, void* stream) {
+  if (limit_us < 1 || limit_us > 2000000 || !err_flag) return PKV_EINVAL;
+  pkv::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(arrive ? 1 : 0,
+                                                                              1000ull * (unsigned long long)limit_us,
+                                                                              err_flag);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    pkv::record_cuda_error(e);
+    return PKV_ECUDA;
+  }
+  return PKV_OK;
+}

@@ -55,14 +55,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase with the given parity to complete.  Gives up after about two
-// seconds (or 2^30 polls) and returns false; the caller reports PKV_DEV_TIMEOUT.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete.  Gives up after limit_ns (about
+// two seconds by default; at most 2^30 polls) and returns false; the caller reports
+// PKV_DEV_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

@@ -1,4 +1,5 @@
-"""Argument checks of the C ABI: bad shapes and sizes return an error, nothing is launched."""
+"""Argument checks of the C ABI (bad shapes and sizes return an error, nothing is launched)
+and the device-side failure detection of the bounded waits."""
 import pytest
 import torch
 
@@ -57,3 +58,29 @@ def test_empty_batch_is_a_no_op():
                 bt=torch.zeros(0, 2, dtype=torch.int32, device=DEV),
                 ctx=torch.zeros(0, dtype=torch.int32, device=DEV))
     assert out.shape == (0, 8, 128)
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """A wait on a barrier nobody arrives at gives up after its limit and reports
+    DEV_TIMEOUT through the flag; a wait whose arrival came first reports nothing; the next
+    attention call on the same context is still correct."""
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pkv.selftest_wait(True, 1000, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    pkv.selftest_wait(False, 2000, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pkv.DEV_TIMEOUT
+    with pytest.raises(pkv.PkvError):
+        pkv.selftest_wait(False, 0, err)
+    import numpy as np
+    import oracle
+    import workloads
+    from gpu_common import check_attention, f64, run_attention
+    w = workloads.make("tiny", 0)
+    kp, vp = workloads.pools_bf16(w, 0)
+    q = workloads.queries(w, 0)
+    ref = oracle.paged_decode_attention(f64(q), f64(kp), f64(vp), w.block_tables, w.context_lens, w.scale,
+                                        w.block_size)
+    out = run_attention(q.to(DEV), kp.to(DEV), vp.to(DEV), w.block_tables, w.context_lens, w.scale, torch.float32)
+    check_attention(out, ref, "after a timed-out wait")
