@@ -92,6 +92,10 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
   // ---------------- producer state (warp-uniform) ----------------
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
+  // ring position of the next issue / the next tile consumed (slot, and the parity of the
+  // pass over the ring), advanced in order instead of dividing by the stage count
+  int p_slot = 0, c_slot = 0;
+  uint32_t p_phase = 0, c_phase = 0;
 
   auto issue = [&](int j) {
     if (cur.s != w_seq || cur.blk < w_base || cur.blk >= w_base + 32) {
@@ -108,10 +112,15 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
       n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
     }
     const int phys = __shfl_sync(FULL_MASK, w_phys, cur.blk - w_base);
+    const int slot = p_slot;
+    const uint32_t ph = p_phase;                               // parity of pass j / S
+    if (++p_slot == S) {
+      p_slot = 0;
+      p_phase ^= 1u;
+    }
     if (lane == 0) {
-      const int slot = j % S;
       bool ok_wait = true;
-      if (j >= S) ok_wait = mbar_wait(&empty[slot], ((j / S) - 1) & 1);
+      if (j >= S) ok_wait = mbar_wait(&empty[slot], ph ^ 1u);   // released in pass j / S - 1
       if (!ok_wait) {
         set_err(a.err, PKV_DEV_TIMEOUT);
         abort_flag = 1;
@@ -174,8 +183,8 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
 
   int consumed = 0;
   for (int j = 0; j < len; ++j) {
-    const int slot = j % S;
-    if (!mbar_wait(&full[slot], (j / S) & 1) || abort_flag) {
+    const int slot = c_slot;
+    if (!mbar_wait(&full[slot], c_phase) || abort_flag) {
       set_err(a.err, PKV_DEV_TIMEOUT);
       abort_flag = 1;
       break;
@@ -381,6 +390,10 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
     if (!PW && warp == 0 && j + S < len) issue(j + S);
+    if (++c_slot == S) {
+      c_slot = 0;
+      c_phase ^= 1u;
+    }
   }
 
   // After a timeout: let this CTA's copies already in flight land before exiting

@@ -245,11 +245,11 @@ __device__ __forceinline__ uint32_t mask_pair_h(uint32_t b, int t, int lead, int
 
 template <int D, int BS>
 __host__ __device__ constexpr size_t int4_smem_bytes(int stages) {
-  return 1024 + (size_t)stages * (Int4Tile<D, BS>::STAGE + 16 + 16);
+  return 128 + (size_t)stages * (Int4Tile<D, BS>::STAGE + 16 + 16);
 }
 
 template <int D, int BS, int NH, int MT>
-__global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 : 0) decode_int4_kernel(const DecodeArgs a) {
   using T = Int4Tile<D, BS>;
   constexpr int TT = BS / 16;       // 16-token tiles per block
   constexpr int KS = D / 16;        // k-steps of K Q^T
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
   constexpr int CV = D / 8;         // V channels per thread (rows of the V^T fragments)
   constexpr int VW = CV / 8;        // V code words per thread per token row
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int S = a.stages;
   int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * T::STAGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + S);
@@ -291,6 +291,23 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
 
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
+  // ring position of the next issue / the next tile consumed (slot, and the parity of the
+  // pass over the ring), advanced in order instead of dividing by the stage count
+  int p_slot = 0, c_slot = 0;
+  uint32_t p_phase = 0, c_phase = 0;
+
+  // Copy roles: lanes 0-3 move a tile's K codes, K metadata, V codes and V metadata (each
+  // array holds one such record per (block, kv head), so its source is base + tile * bytes).
+  const uint8_t* cp_base = nullptr;
+  uint32_t cp_bytes = 0, cp_off = 0;
+  if (lane == 0) { cp_base = a.k_codes; cp_bytes = BS * D / 2; cp_off = T::KC; }
+  if (lane == 1) { cp_base = reinterpret_cast<const uint8_t*>(a.k_meta); cp_bytes = 4 * D; cp_off = T::KM; }
+  if (lane == 2) { cp_base = a.v_codes; cp_bytes = BS * D / 2; cp_off = T::VC; }
+  if (lane == 3) { cp_base = reinterpret_cast<const uint8_t*>(a.v_meta); cp_bytes = 4 * BS; cp_off = T::VM; }
+  const uint32_t ring_sa = smem_u32(smem) + cp_off;
+  // constants of the segment the producer is in, set when it enters one: its last block,
+  // and pack_rows(rows of the last block, rows of block 0 before the window, F_WHOLE)
+  int seg_last = 0, seg_rows = 0;
 
   auto issue = [&](int j) {
     if (cur.s != w_seq || cur.blk < w_base || cur.blk >= w_base + 32) {
@@ -307,48 +324,54 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
       n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
     }
     const int phys = __shfl_sync(FULL_MASK, w_phys, cur.blk - w_base);
+    const int slot = p_slot;
+    const uint32_t ph = p_phase;                               // parity of pass j / S
+    if (++p_slot == S) {
+      p_slot = 0;
+      p_phase ^= 1u;
+    }
+    const bool first = j == 0 || cur.blk == 0;
+    if (first) {
+      seg_last = cur.nb - 1;
+      seg_rows = pack_rows(cur.ctx - (cur.b0 + seg_last) * BS, window_lead(cur.ctx, a.window, BS),
+                           cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend ? F_WHOLE : 0);
+      const char* qp = reinterpret_cast<const char*>(a.q) + ((size_t)cur.s * a.n_h + (size_t)cur.g * a.G) * D * 2;
+      for (int off = lane * 128; off < a.G * D * 2; off += 32 * 128) prefetch_l2(qp + off);
+      if (cur.ctx % BS) {                                      // warm L2 with the bf16 tail early
+        const char* tail = reinterpret_cast<const char*>(a.k_tail + ((size_t)cur.s * a.n_kv + cur.g) * BS * D);
+        for (int off = lane * 128; off < 2 * BS * D; off += 32 * 128) prefetch_l2(tail + off);
+      }
+    }
+    // A single consumer warp is this warp: the slot refilled here is the one it released
+    // just before (after __syncwarp, every value read from it already used), so only the
+    // order of its generic-proxy reads before the async-proxy writes is needed.  Several
+    // consumer warps release the slot through the empty barrier.
+    bool ok_wait = true;
+    if (MT > 1 && j >= S) {
+      if (lane == 0) ok_wait = mbar_wait(&empty[slot], ph ^ 1u);   // released in pass j / S - 1
+      ok_wait = __shfl_sync(FULL_MASK, ok_wait, 0);
+    }
+    const bool last = cur.blk == seg_last;
+    const int ntok = last ? (seg_rows & 255) : BS;
+    const bool ok = (unsigned)phys < (unsigned)a.num_blocks, go = ok && ok_wait, whole_blk = ntok == BS;
+    const int flags = (seg_rows >> 8 & F_WHOLE) | (ok ? F_VALID : 0) | (first ? F_FIRST : 0) |
+                      (last || j == len - 1 ? F_LAST : 0);
     if (lane == 0) {
-      const int slot = j % S;
-      bool ok_wait = true;
-      if (j >= S) ok_wait = mbar_wait(&empty[slot], ((j / S) - 1) & 1);
       if (!ok_wait) {
         set_err(a.err, PKV_DEV_TIMEOUT);
         abort_flag = 1;
       }
-      const int ntok = cur.blk == cur.nb - 1 ? cur.ctx - (cur.b0 + cur.blk) * BS : BS;
-      const int lead = cur.blk == 0 ? window_lead(cur.ctx, a.window, BS) : 0;
-      int flags = 0;
-      if (j == 0 || cur.blk == 0) flags |= F_FIRST;
-      if (j == len - 1 || cur.blk == cur.nb - 1) flags |= F_LAST;
-      if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
-      const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
-      if (ok) flags |= F_VALID; else set_err(a.err, PKV_DEV_BAD_BLOCK);
-      meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, lead, flags));
-      const char* tail = reinterpret_cast<const char*>(a.k_tail + ((size_t)cur.s * a.n_kv + cur.g) * BS * D);
-      if (ok && ok_wait) {
-        uint8_t* st = smem + (size_t)slot * T::STAGE;
-        const size_t tile = (size_t)phys * a.n_kv + cur.g;
-        if (ntok == BS) {
-          mbar_arrive_expect_tx(&full[slot], T::FULL_BYTES);
-          bulk_g2s(st + T::KC, a.k_codes + tile * (BS * D / 2), BS * D / 2, &full[slot], pol);
-          bulk_g2s(st + T::KM, a.k_meta + tile * (2 * D), 4 * D, &full[slot], pol);
-        } else {
-          // the sequence's unfinished block: K comes from its bf16 tail (read by the
-          // consumers straight from L2), V from the codes
-          mbar_arrive_expect_tx(&full[slot], T::TAIL_BYTES);
-          for (int off = 0; off < 2 * BS * D; off += 128) prefetch_l2(tail + off);
-        }
-        bulk_g2s(st + T::VC, a.v_codes + tile * (BS * D / 2), BS * D / 2, &full[slot], pol);
-        bulk_g2s(st + T::VM, a.v_meta + tile * (2 * BS), 4 * BS, &full[slot], pol);
-      } else {
-        mbar_arrive(&full[slot]);
-      }
-      if (flags & F_FIRST) {
-        const char* qp = reinterpret_cast<const char*>(a.q) + ((size_t)cur.s * a.n_h + (size_t)cur.g * a.G) * D * 2;
-        for (int off = 0; off < a.G * D * 2; off += 128) prefetch_l2(qp + off);
-        if (cur.ctx % BS)                                      // warm L2 with the tail early
-          for (int off = 0; off < 2 * BS * D; off += 128) prefetch_l2(tail + off);
-      }
+      if (!ok) set_err(a.err, PKV_DEV_BAD_BLOCK);
+      meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, cur.blk == 0 ? seg_rows >> 16 : 0, flags));
+      if (go) mbar_arrive_expect_tx(&full[slot], whole_blk ? T::FULL_BYTES : T::TAIL_BYTES);
+      else mbar_arrive(&full[slot]);
+    }
+    // the unfinished block's K comes from its bf16 tail (read by the consumers from L2)
+    if (go && cp_bytes != 0 && (whole_blk || lane >= 2)) {
+      const size_t tile = (size_t)(unsigned)phys * (unsigned)a.n_kv + (unsigned)cur.g;
+      if (MT == 1 && j >= S) fence_proxy_async_smem();
+      bulk_g2s_u32(ring_sa + (uint32_t)slot * T::STAGE, cp_base + tile * cp_bytes, cp_bytes, smem_u32(&full[slot]),
+                   pol);
     }
     if (j + 1 < len) cursor_next(cur, a);
   };
@@ -375,8 +398,8 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
 
   int consumed = 0;
   for (int j = 0; j < len; ++j) {
-    const int slot = j % S;
-    if (!mbar_wait(&full[slot], (j / S) & 1) || abort_flag) {
+    const int slot = c_slot;
+    if (!mbar_wait(&full[slot], c_phase) || abort_flag) {
       set_err(a.err, PKV_DEV_TIMEOUT);
       abort_flag = 1;
       break;
@@ -642,8 +665,12 @@ __global__ void __launch_bounds__(MT * 32) decode_int4_kernel(const DecodeArgs a
     }
 
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (MT > 1 && lane == 0) mbar_arrive(&empty[slot]);
     if (warp == 0 && j + S < len) issue(j + S);
+    if (++c_slot == S) {
+      c_slot = 0;
+      c_phase ^= 1u;
+    }
   }
 
   if (abort_flag && threadIdx.x == 0) {
@@ -666,7 +693,7 @@ template <int D, int BS, int NH, int MT>
 static Int4Variant make_int4_variant() {
   Int4Variant v;
   v.fn = (const void*)decode_int4_kernel<D, BS, NH, MT>;
-  v.stages = ring_stages(Int4Tile<D, BS>::STAGE, 16384, "PKV_STAGES_INT4");
+  v.stages = ring_stages(Int4Tile<D, BS>::STAGE, BS == 16 ? 11264 : 16384, "PKV_STAGES_INT4");
   v.smem = int4_smem_bytes<D, BS>(v.stages);
   v.warps = MT;
   v.P = 0;
