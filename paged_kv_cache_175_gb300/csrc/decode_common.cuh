@@ -17,6 +17,11 @@
 namespace pkv {
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_VALID = 8 };
+// Lazy softmax offset (base-2 units): the attention kernels raise a head's running offset
+// only when a score exceeds it by more than this, so exponentials stay below 2^8 (inside
+// the range of the fp16 high + low split of P) and most tiles skip the max reduction and
+// the rescale.  Softmax itself does not depend on the offset.
+constexpr float kLazyMax = 8.f;
 
 struct DecodeArgs {
   const void* q;                 // bf16 [B][n_h][D]
@@ -217,6 +222,72 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const DecodeArgs& a) {
     c.ctx = a.ctx_eff[c.s];
   }
   c.b0 = window_first_block(c.ctx, a.window, a.block_size);
+}
+
+// One tile's step of the online softmax over tokens (rows of the token-major S^T tiles),
+// per head (column), base 2: sc holds the raw scores of TT 16-token tiles x NH 8-head
+// tiles in the m16n8 accumulator layout (thread: tokens gid, gid + 8; heads 2*tig + e).
+// Scores are scaled, rows outside [lead, ntok) masked, and sc is replaced by the
+// exponentials; l and the O^T accumulators are rescaled when the offset rises.
+template <int TT, int NH, int MD>
+__device__ __forceinline__ void softmax_tile(float (&sc)[TT][NH][4], float (&m)[NH][2], float (&l)[NH][2],
+                                             float (&o)[MD][NH][4], int gid, int ntok, int lead, float scale_log2) {
+  // Exponents are taken against the running offset m, raised (to the exact running max,
+  // with the rescale of l and O) only when a score exceeds it by more than kLazyMax.
+  bool over = false;
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int tok = t * 16 + gid + 8 * r;
+          float x = sc[t][nh][2 * r + e] * scale_log2;
+          if (tok >= ntok || tok < lead) x = -INFINITY;
+          sc[t][nh][2 * r + e] = x;
+          over |= x > m[nh][e] + kLazyMax;
+        }
+  if (__any_sync(FULL_MASK, over)) {
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) {
+      float al[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) mx = fmaxf(mx, fmaxf(sc[t][nh][e], sc[t][nh][2 + e]));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+        const float mn = fmaxf(m[nh][e], mx);
+        al[e] = ex2(m[nh][e] - mn);
+        m[nh][e] = mn;
+        l[nh][e] *= al[e];
+      }
+#pragma unroll
+      for (int md = 0; md < MD; ++md) {
+        o[md][nh][0] *= al[0]; o[md][nh][1] *= al[1];
+        o[md][nh][2] *= al[0]; o[md][nh][3] *= al[1];
+      }
+    }
+  }
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float rs = 0.f;
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float pv = ex2(sc[t][nh][2 * r + e] - m[nh][e]);
+          sc[t][nh][2 * r + e] = pv;
+          rs += pv;
+        }
+      l[nh][e] += rs;
+    }
 }
 
 // Host launchers (decode_plan.cu).

@@ -515,52 +515,7 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
           for (int i = 0; i < 4; ++i) sc[t][nh][i] += sx[t][nh][i];
-      // ---- online softmax over tokens (rows), per head (column), base 2 ----
-      float al[NH][2];
-      bool rescale = false;
-#pragma unroll
-      for (int nh = 0; nh < NH; ++nh) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int t = 0; t < TT; ++t)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int tok = t * 16 + gid + 8 * r;
-              float x = sc[t][nh][2 * r + e] * a.scale_log2;
-              if (tok >= ntok || tok < lead) x = -INFINITY;
-              sc[t][nh][2 * r + e] = x;
-              mx = fmaxf(mx, x);
-            }
-          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
-          const float mn = fmaxf(m[nh][e], mx);
-          al[nh][e] = ex2(m[nh][e] - mn);
-          rescale |= al[nh][e] != 1.f;
-          m[nh][e] = mn;
-          float rs = 0.f;
-#pragma unroll
-          for (int t = 0; t < TT; ++t)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float pv = ex2(sc[t][nh][2 * r + e] - mn);
-              sc[t][nh][2 * r + e] = pv;
-              rs += pv;
-            }
-          l[nh][e] = l[nh][e] * al[nh][e] + rs;
-        }
-      }
-      if (__any_sync(FULL_MASK, rescale)) {
-#pragma unroll
-        for (int md = 0; md < MD; ++md)
-#pragma unroll
-          for (int nh = 0; nh < NH; ++nh) {
-            o[md][nh][0] *= al[nh][0]; o[md][nh][1] *= al[nh][1];
-            o[md][nh][2] *= al[nh][0]; o[md][nh][3] *= al[nh][1];
-          }
-      }
+      softmax_tile<TT, NH, MD>(sc, m, l, o, gid, ntok, lead, a.scale_log2);
       // ---- O^T += V^T P^T (fp16, P as high + low) ----
       const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + T::VM);
 #pragma unroll
