@@ -177,11 +177,17 @@ pkv_status pkv_paged_decode_attn_noalloc(const void* q, const void* k_pool, cons
  *   k, v          bf16 [n_tok][n_kv][head_dim]
  *   slot_mapping  int64 [n_tok] (negative = padding); tail_seq int32 [n_tok]: the
  *                 tail row (batch index) of each token's sequence, in [0, tail_rows).
- *   k_codes, v_codes  uint8 [num_blocks][n_kv][block_size][head_dim/2]: 8 channels
- *                 per little-endian 32-bit word, nibble n of word w holds channel
- *                 8w + (0,2,4,6,1,3,5,7)[n] (even channels in the low half-word).
- *   k_meta        fp16 [num_blocks][n_kv][2][head_dim]: scale row, then min row.
- *   v_meta        fp16 [num_blocks][n_kv][block_size][2]: (scale, min) per token.
+ *   cache         uint8 [num_blocks][n_kv][R], R = pkv_int4_record_bytes(block_size,
+ *                 head_dim): one record per (block, kv head), read by the attention
+ *                 kernel as one contiguous copy.  Byte offsets inside a record:
+ *                   0              K codes  [block_size][head_dim/2]
+ *                   bs*d/2         V codes  [block_size][head_dim/2]
+ *                   bs*d           K meta   fp16 [2][head_dim]: scale row, then min row
+ *                   bs*d + 4d      V meta   fp16 [block_size][2]: (scale, min) per token
+ *                 A code row packs 8 channels per little-endian 32-bit word: nibble n of
+ *                 word w holds channel 8w + (0,2,4,6,1,3,5,7)[n] (even channels in the
+ *                 low half-word).  The K codes and K meta of a block not yet full are
+ *                 not defined.
  *   k_tail        bf16 [tail_rows][n_kv][block_size][head_dim].
  * Caller contract: slots distinct; within one call the tokens of a sequence are
  * consecutive entries in logical order with one tail_seq; a sequence starts at
@@ -189,24 +195,29 @@ pkv_status pkv_paged_decode_attn_noalloc(const void* q, const void* k_pool, cons
  * Enqueues two kernels (quantize, then tail update) on `stream`.
  */
 pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, const int64_t* slot_mapping,
-                                    const int32_t* tail_seq, int n_tok, uint8_t* k_codes,
-                                    void* k_meta, uint8_t* v_codes, void* v_meta, void* k_tail,
+                                    const int32_t* tail_seq, int n_tok, uint8_t* cache, void* k_tail,
                                     int tail_rows, int num_blocks, int block_size, int n_kv,
                                     int head_dim, int32_t* err_flag, void* stream);
+
+/*
+ * Bytes of one (block, kv head) record of the INT4 cache: block_size * head_dim (codes
+ * of K and V) + 4 * head_dim (K scale and min rows) + 4 * block_size (V scale and min per
+ * token); a multiple of 16.  0 on a shape the INT4 kernels do not take.
+ */
+size_t pkv_int4_record_bytes(int block_size, int head_dim);
 
 /*
  * paged_decode_attn_int4 — decode attention over the INT4 cache written by
  * pkv_kv_quant_append_int4.  Full blocks are dequantized in registers (K and V
  * to fp16, x^ = code * s + m); the last, unfinished block of sequence s takes
  * its K rows from k_tail[s] (bf16) and its V rows from the codes.
- * Same arguments and output as pkv_paged_decode_attn, with the INT4 tensors in
- * place of the pools; the batch index is the tail row.  q.k and p.v use fp16
+ * Same arguments and output as pkv_paged_decode_attn, with the INT4 cache and the
+ * K tail in place of the pools; the batch index is the tail row.  q.k and p.v use fp16
  * tensor-core mma with fp32 accumulation (q converted to fp16 once; p carried as an
  * fp16 high + low pair).  The dequantized values, q and the tail must lie in fp16 range.
  */
-pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, const void* k_meta,
-                                      const uint8_t* v_codes, const void* v_meta,
-                                      const void* k_tail, const int32_t* block_tables,
+pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* cache, const void* k_tail,
+                                      const int32_t* block_tables,
                                       int max_blocks, const int32_t* context_lens, float scale,
                                       int batch, int n_h, int n_kv, int head_dim, int block_size,
                                       int num_blocks, void* out, int out_dtype, void* workspace,
@@ -215,12 +226,11 @@ pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, con
 /*
  * paged_decode_attn_int4_window — pkv_paged_decode_attn_int4 over the last `window`
  * tokens of each context (0: the whole context), with the window read as for
- * pkv_paged_decode_attn_window: K/V codes, metadata and table entries of blocks that end
- * before the window are not read.
+ * pkv_paged_decode_attn_window: the records and table entries of blocks that end before
+ * the window are not read.
  */
-pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uint8_t* k_codes, const void* k_meta,
-                                             const uint8_t* v_codes, const void* v_meta,
-                                             const void* k_tail, const int32_t* block_tables,
+pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uint8_t* cache, const void* k_tail,
+                                             const int32_t* block_tables,
                                              int max_blocks, const int32_t* context_lens, float scale,
                                              int window, int batch, int n_h, int n_kv, int head_dim,
                                              int block_size, int num_blocks, void* out, int out_dtype,

@@ -38,16 +38,17 @@ _SIGS = {
     "pkv_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "pkv_paged_decode_attn": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
                                    _P, _I, _P, ctypes.c_size_t, _P, _P]),
-    "pkv_kv_quant_append_int4": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
-    "pkv_paged_decode_attn_int4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I,
-                                        _I, _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pkv_kv_quant_append_int4": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pkv_int4_record_bytes": (ctypes.c_size_t, [_I, _I]),
+    "pkv_paged_decode_attn_int4": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
+                                        _P, _I, _P, ctypes.c_size_t, _P, _P]),
     "pkv_rope_shift_k": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_double, _P, _P]),
     "pkv_paged_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
                                            _P, _I, _P, _P]),
     "pkv_paged_decode_attn_window": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I, _I,
                                           _P, _I, _P, ctypes.c_size_t, _P, _P]),
-    "pkv_paged_decode_attn_int4_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I,
-                                               _I, _I, _I, _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pkv_paged_decode_attn_int4_window": (_I, [_P, _P, _P, _P, _I, _P, ctypes.c_float, _I, _I, _I, _I, _I, _I,
+                                               _I, _P, _I, _P, ctypes.c_size_t, _P, _P]),
     # block manager (host) and its copy executor
     "pkv_bm_create": (_P, [_I, _I, _I, _I, _I]),
     "pkv_bm_destroy": (None, [_P]),
@@ -206,40 +207,65 @@ def paged_decode_attn_noalloc(q, k_pool, v_pool, block_tables, context_lens, sca
     return out
 
 
+def int4_record_bytes(block_size, head_dim) -> int:
+    """Bytes of one (block, kv head) record of the INT4 cache (0 for an unsupported shape)."""
+    return int(lib().pkv_int4_record_bytes(int(block_size), int(head_dim)))
+
+
 @dataclass
 class Int4CacheTensors:
-    k_codes: torch.Tensor     # uint8 [num_blocks][n_kv][bs][d/2]
-    k_meta: torch.Tensor      # fp16  [num_blocks][n_kv][2][d]
-    v_codes: torch.Tensor     # uint8 [num_blocks][n_kv][bs][d/2]
-    v_meta: torch.Tensor      # fp16  [num_blocks][n_kv][bs][2]
+    """INT4 paged cache: one record per (block, kv head) -- K codes, V codes, K scale and
+    min rows, V (scale, min) per token -- plus the bf16 K rows of unfinished blocks.  The
+    four fields of the records are exposed as views."""
+    records: torch.Tensor     # uint8 [num_blocks][n_kv][int4_record_bytes(bs, d)]
     k_tail: torch.Tensor      # bf16  [tail_rows][n_kv][bs][d]
 
     @property
     def shape(self):
-        nb, n_kv, bs, dh = self.k_codes.shape
-        return nb, n_kv, bs, dh * 2
+        _, n_kv, bs, d = self.k_tail.shape
+        return self.records.shape[0], n_kv, bs, d
+
+    def _field(self, start, size):
+        return self.records[:, :, start:start + size]
+
+    @property
+    def k_codes(self):         # uint8 [num_blocks][n_kv][bs][d/2]
+        nb, n_kv, bs, d = self.shape
+        return self._field(0, bs * d // 2).view(nb, n_kv, bs, d // 2)
+
+    @property
+    def v_codes(self):         # uint8 [num_blocks][n_kv][bs][d/2]
+        nb, n_kv, bs, d = self.shape
+        return self._field(bs * d // 2, bs * d // 2).view(nb, n_kv, bs, d // 2)
+
+    @property
+    def k_meta(self):          # fp16 [num_blocks][n_kv][2][d]: scale row, min row
+        nb, n_kv, bs, d = self.shape
+        return self._field(bs * d, 4 * d).view(torch.float16).view(nb, n_kv, 2, d)
+
+    @property
+    def v_meta(self):          # fp16 [num_blocks][n_kv][bs][2]: (scale, min) per token
+        nb, n_kv, bs, d = self.shape
+        return self._field(bs * d + 4 * d, 4 * bs).view(torch.float16).view(nb, n_kv, bs, 2)
 
 
 def alloc_int4_cache(num_blocks, n_kv, block_size, head_dim, tail_rows, device="cuda") -> Int4CacheTensors:
-    z = dict(device=device)
-    return Int4CacheTensors(
-        torch.zeros(num_blocks, n_kv, block_size, head_dim // 2, dtype=torch.uint8, **z),
-        torch.zeros(num_blocks, n_kv, 2, head_dim, dtype=torch.float16, **z),
-        torch.zeros(num_blocks, n_kv, block_size, head_dim // 2, dtype=torch.uint8, **z),
-        torch.zeros(num_blocks, n_kv, block_size, 2, dtype=torch.float16, **z),
-        torch.zeros(tail_rows, n_kv, block_size, head_dim, dtype=torch.bfloat16, **z))
+    rec = int4_record_bytes(block_size, head_dim)
+    if rec == 0:
+        raise ValueError(f"INT4 cache: unsupported block_size {block_size} / head_dim {head_dim}")
+    return Int4CacheTensors(torch.zeros(num_blocks, n_kv, rec, dtype=torch.uint8, device=device),
+                            torch.zeros(tail_rows, n_kv, block_size, head_dim, dtype=torch.bfloat16, device=device))
 
 
 def kv_quant_append_int4(k, v, slot_mapping, tail_seq, cache: Int4CacheTensors, err=None, stream=None):
     """Quantize-on-append of k, v [n_tok][n_kv][d] into the INT4 cache."""
-    _cuda(k, v, slot_mapping, tail_seq, cache.k_codes, cache.k_meta, cache.v_codes, cache.v_meta, cache.k_tail, err)
+    _cuda(k, v, slot_mapping, tail_seq, cache.records, cache.k_tail, err)
     assert k.dtype == v.dtype == torch.bfloat16 and slot_mapping.dtype == torch.int64
     assert tail_seq.dtype == torch.int32
     nb, n_kv, bs, d = cache.shape
     _check("kv_quant_append_int4", lib().pkv_kv_quant_append_int4(
-        _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(tail_seq), k.shape[0], _ptr(cache.k_codes), _ptr(cache.k_meta),
-        _ptr(cache.v_codes), _ptr(cache.v_meta), _ptr(cache.k_tail), cache.k_tail.shape[0], nb, bs, n_kv, d,
-        _ptr(err), _stream(stream)))
+        _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(tail_seq), k.shape[0], _ptr(cache.records), _ptr(cache.k_tail),
+        cache.k_tail.shape[0], nb, bs, n_kv, d, _ptr(err), _stream(stream)))
 
 
 def paged_decode_attn_int4(q, cache: Int4CacheTensors, block_tables, context_lens, scale, out=None,
@@ -267,14 +293,12 @@ def _decode_int4(q, cache, block_tables, context_lens, scale, window, out, out_d
         workspace = _workspace(need, q.device)
     if window == 0:
         _check("paged_decode_attn_int4", lib().pkv_paged_decode_attn_int4(
-            _ptr(q), _ptr(cache.k_codes), _ptr(cache.k_meta), _ptr(cache.v_codes), _ptr(cache.v_meta),
-            _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), B,
-            n_h, n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
+            _ptr(q), _ptr(cache.records), _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1],
+            _ptr(context_lens), float(scale), B, n_h, n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
     else:
         _check("paged_decode_attn_int4_window", lib().pkv_paged_decode_attn_int4_window(
-            _ptr(q), _ptr(cache.k_codes), _ptr(cache.k_meta), _ptr(cache.v_codes), _ptr(cache.v_meta),
-            _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale),
-            window, B, n_h, n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err),
+            _ptr(q), _ptr(cache.records), _ptr(cache.k_tail), _ptr(block_tables), block_tables.shape[1],
+            _ptr(context_lens), float(scale), window, B, n_h, n_kv, d, bs, nb, _ptr(out), od, _ptr(workspace), workspace.numel(), _ptr(err),
             _stream(stream)))
     return out
 

@@ -43,11 +43,8 @@ struct DecodeArgs {
   const int32_t* ctx_raw;
   int max_ctx, block_size, inline_plan;
   int window;                    // attention window in tokens (0: the whole context)
-  // INT4 cache (unused by the bf16 kernel)
-  const uint8_t* k_codes;
-  const uint8_t* v_codes;
-  const __half* k_meta;
-  const __half* v_meta;
+  // INT4 cache (unused by the bf16 kernel): (block, kv head) records and the bf16 K tail
+  const uint8_t* cache;
   const __nv_bfloat16* k_tail;
 };
 

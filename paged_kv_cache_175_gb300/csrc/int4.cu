@@ -55,10 +55,8 @@ struct QuantAppendArgs {
   const int32_t* tail_seq;
   int n_tok, n_kv, block_size, tail_rows;
   long long n_slots;
-  uint8_t* k_codes;
-  __half* k_meta;
-  uint8_t* v_codes;
-  __half* v_meta;
+  uint8_t* cache;                 // [num_blocks][n_kv][rec_bytes] records
+  size_t rec_bytes;
   __nv_bfloat16* k_tail;
   int32_t* err;
 };
@@ -85,6 +83,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
   const long long blk = slot / BS;
   const int row = (int)(slot - blk * BS);
   const size_t tile = (size_t)blk * a.n_kv + g;           // (block, kv head)
+  uint8_t* rec = a.cache + tile * a.rec_bytes;            // K codes, V codes, K meta, V meta
 
   // ---- V: per token ----
   {
@@ -106,11 +105,11 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
     }
 #pragma unroll
     for (int o = 1; o < LPW; o <<= 1) word |= __shfl_xor_sync(FULL_MASK, word, o);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(a.v_codes + (tile * BS + row) * (D / 2));
+    uint32_t* dst = reinterpret_cast<uint32_t*>(rec + (size_t)(BS + row) * (D / 2));
     if (lane % LPW == 0) dst[lane / LPW] = word;
     if (lane == 0) {
       __half2 meta = __halves2half2(q.s16, q.m16);
-      reinterpret_cast<__half2*>(a.v_meta)[tile * BS + row] = meta;
+      reinterpret_cast<__half2*>(rec + (size_t)BS * D + 4 * D)[row] = meta;
     }
   }
 
@@ -135,8 +134,8 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
   const int first_call_row = BS - 1 - run;
   const __nv_bfloat16* krow_call = a.k + g * D;            // token t: + t * n_kv * D
   const __nv_bfloat16* krow_tail = a.k_tail + ((size_t)seq * a.n_kv + g) * BS * D;
-  __half* kmeta = a.k_meta + tile * 2 * D;
-  uint32_t* kcodes = reinterpret_cast<uint32_t*>(a.k_codes + tile * BS * (D / 2));
+  __half* kmeta = reinterpret_cast<__half*>(rec + (size_t)BS * D);
+  uint32_t* kcodes = reinterpret_cast<uint32_t*>(rec);
 #pragma unroll 1
   for (int cm = 0; cm < CPL; ++cm) {
     const int c = lane + 32 * cm;                            // this lane's channel
@@ -191,11 +190,10 @@ __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a
 // Decode attention over the INT4 cache.
 //
 // Same partition, producer and token-major tiles as the bf16 kernel.  A stage holds one
-// (block, kv head): K codes [BS][D/2], V codes [BS][D/2], K meta [2][D] fp16 and V meta
-// [BS][2] fp16, each one 1-D bulk copy.  A sequence's unfinished last block has no K
-// codes: its K rows are read from the bf16 tail straight from L2 (the producer
-// prefetches them when the segment starts and again when it issues the block), so the
-// ring holds no tail space.
+// (block, kv head) record -- K codes [BS][D/2], V codes [BS][D/2], K meta [2][D] fp16,
+// V meta [BS][2] fp16 -- moved by one 1-D bulk copy.  A sequence's unfinished last block
+// has no K codes: its K rows are read from the bf16 tail straight from L2 (the producer
+// prefetches them when it enters the segment), so the ring holds no tail space.
 //
 // S^T = K^ Q^T uses fp16 mma.  The channel order inside a k-step is chosen so each
 // thread's A-fragment rows come from one 16-byte load of a token row: thread t of a quad
@@ -217,9 +215,8 @@ struct Int4Tile {
   static constexpr int VC = BS * D / 2;                     // V codes [BS][D/2]
   static constexpr int KM = BS * D;                         // K meta [2][D] fp16
   static constexpr int VM = BS * D + 4 * D;                 // V meta [BS][2] fp16
-  static constexpr int STAGE = (BS * D + 4 * D + 4 * BS + 127) / 128 * 128;
-  static constexpr int FULL_BYTES = BS * D + 4 * D + 4 * BS;          // codes + metadata
-  static constexpr int TAIL_BYTES = BS * D / 2 + 4 * BS;              // V codes + V meta
+  static constexpr int REC = BS * D + 4 * D + 4 * BS;                 // one cache record
+  static constexpr int STAGE = (REC + 127) / 128 * 128;
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -296,15 +293,7 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
   int p_slot = 0, c_slot = 0;
   uint32_t p_phase = 0, c_phase = 0;
 
-  // Copy roles: lanes 0-3 move a tile's K codes, K metadata, V codes and V metadata (each
-  // array holds one such record per (block, kv head), so its source is base + tile * bytes).
-  const uint8_t* cp_base = nullptr;
-  uint32_t cp_bytes = 0, cp_off = 0;
-  if (lane == 0) { cp_base = a.k_codes; cp_bytes = BS * D / 2; cp_off = T::KC; }
-  if (lane == 1) { cp_base = reinterpret_cast<const uint8_t*>(a.k_meta); cp_bytes = 4 * D; cp_off = T::KM; }
-  if (lane == 2) { cp_base = a.v_codes; cp_bytes = BS * D / 2; cp_off = T::VC; }
-  if (lane == 3) { cp_base = reinterpret_cast<const uint8_t*>(a.v_meta); cp_bytes = 4 * BS; cp_off = T::VM; }
-  const uint32_t ring_sa = smem_u32(smem) + cp_off;
+  const uint32_t ring_sa = smem_u32(smem);                   // ring, then meta[S], then full[S]
   // constants of the segment the producer is in, set when it enters one: its last block,
   // and pack_rows(rows of the last block, rows of block 0 before the window, F_WHOLE)
   int seg_last = 0, seg_rows = 0;
@@ -353,7 +342,7 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
     }
     const bool last = cur.blk == seg_last;
     const int ntok = last ? (seg_rows & 255) : BS;
-    const bool ok = (unsigned)phys < (unsigned)a.num_blocks, go = ok && ok_wait, whole_blk = ntok == BS;
+    const bool ok = (unsigned)phys < (unsigned)a.num_blocks, go = ok && ok_wait;
     const int flags = (seg_rows >> 8 & F_WHOLE) | (ok ? F_VALID : 0) | (first ? F_FIRST : 0) |
                       (last || j == len - 1 ? F_LAST : 0);
     if (lane == 0) {
@@ -363,15 +352,16 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
       }
       if (!ok) set_err(a.err, PKV_DEV_BAD_BLOCK);
       meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, cur.blk == 0 ? seg_rows >> 16 : 0, flags));
-      if (go) mbar_arrive_expect_tx(&full[slot], whole_blk ? T::FULL_BYTES : T::TAIL_BYTES);
-      else mbar_arrive(&full[slot]);
-    }
-    // the unfinished block's K comes from its bf16 tail (read by the consumers from L2)
-    if (go && cp_bytes != 0 && (whole_blk || lane >= 2)) {
-      const size_t tile = (size_t)(unsigned)phys * (unsigned)a.n_kv + (unsigned)cur.g;
-      if (MT == 1 && j >= S) fence_proxy_async_smem();
-      bulk_g2s_u32(ring_sa + (uint32_t)slot * T::STAGE, cp_base + tile * cp_bytes, cp_bytes, smem_u32(&full[slot]),
-                   pol);
+      if (go) {
+        // the whole record, also for the unfinished block (its K codes are then unused)
+        mbar_arrive_expect_tx(&full[slot], T::REC);
+        if (MT == 1 && j >= S) fence_proxy_async_smem();
+        bulk_g2s_u32(ring_sa + (uint32_t)slot * T::STAGE,
+                     a.cache + ((size_t)(unsigned)phys * (unsigned)a.n_kv + (unsigned)cur.g) * T::REC, T::REC,
+                     ring_sa + S * (T::STAGE + 16) + 8u * (uint32_t)slot, pol);
+      } else {
+        mbar_arrive(&full[slot]);
+      }
     }
     if (j + 1 < len) cursor_next(cur, a);
   };
@@ -701,19 +691,21 @@ static bool valid_shape(int n_h, int n_kv, int head_dim, int block_size) {
   return n_h / n_kv <= 64;
 }
 
+extern "C" size_t pkv_int4_record_bytes(int block_size, int head_dim) {
+  if (head_dim != 64 && head_dim != 128) return 0;
+  if (block_size != 16 && block_size != 32 && block_size != 64) return 0;
+  return (size_t)block_size * head_dim + 4 * (size_t)head_dim + 4 * (size_t)block_size;
+}
+
 extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, const int64_t* slot_mapping,
-                                               const int32_t* tail_seq, int n_tok, uint8_t* k_codes, void* k_meta,
-                                               uint8_t* v_codes, void* v_meta, void* k_tail, int tail_rows,
-                                               int num_blocks, int block_size, int n_kv, int head_dim,
-                                               int32_t* err_flag, void* stream) {
+                                               const int32_t* tail_seq, int n_tok, uint8_t* cache, void* k_tail,
+                                               int tail_rows, int num_blocks, int block_size, int n_kv,
+                                               int head_dim, int32_t* err_flag, void* stream) {
   if (n_tok < 0 || num_blocks < 0 || n_kv <= 0 || tail_rows < 0) return PKV_EINVAL;
-  if (head_dim != 64 && head_dim != 128) return PKV_EINVAL;
-  if (block_size != 16 && block_size != 32 && block_size != 64) return PKV_EINVAL;
+  if (pkv_int4_record_bytes(block_size, head_dim) == 0) return PKV_EINVAL;
   if (n_tok == 0) return PKV_OK;
-  if (!k || !v || !slot_mapping || !tail_seq || !k_codes || !k_meta || !v_codes || !v_meta || !k_tail)
-    return PKV_EINVAL;
-  if (!al16(k) || !al16(v) || !al16(k_codes) || !al16(v_codes) || !al16(k_meta) || !al16(v_meta) || !al16(k_tail))
-    return PKV_EINVAL;
+  if (!k || !v || !slot_mapping || !tail_seq || !cache || !k_tail) return PKV_EINVAL;
+  if (!al16(k) || !al16(v) || !al16(cache) || !al16(k_tail)) return PKV_EINVAL;
   QuantAppendArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -724,10 +716,8 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
   a.block_size = block_size;
   a.tail_rows = tail_rows;
   a.n_slots = (long long)num_blocks * block_size;
-  a.k_codes = k_codes;
-  a.k_meta = static_cast<__half*>(k_meta);
-  a.v_codes = v_codes;
-  a.v_meta = static_cast<__half*>(v_meta);
+  a.cache = cache;
+  a.rec_bytes = pkv_int4_record_bytes(block_size, head_dim);
   a.k_tail = static_cast<__nv_bfloat16*>(k_tail);
   a.err = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -750,8 +740,8 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
   return PKV_OK;
 }
 
-static pkv_status decode_int4(const void* q, const uint8_t* k_codes, const void* k_meta, const uint8_t* v_codes,
-                              const void* v_meta, const void* k_tail, const int32_t* block_tables, int max_blocks,
+static pkv_status decode_int4(const void* q, const uint8_t* cache, const void* k_tail, const int32_t* block_tables,
+                              int max_blocks,
                               const int32_t* context_lens, float scale, int window, int batch, int n_h, int n_kv,
                               int head_dim, int block_size, int num_blocks, void* out, int out_dtype, void* workspace,
                               size_t workspace_bytes, int32_t* err_flag, void* stream) {
@@ -759,11 +749,8 @@ static pkv_status decode_int4(const void* q, const uint8_t* k_codes, const void*
     return PKV_EINVAL;
   if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_F32) return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
-  if (!q || !k_codes || !k_meta || !v_codes || !v_meta || !k_tail || !block_tables || !context_lens || !out ||
-      !workspace)
-    return PKV_EINVAL;
-  if (!al16(q) || !al16(k_codes) || !al16(v_codes) || !al16(k_meta) || !al16(v_meta) || !al16(k_tail) ||
-      !al16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  if (!q || !cache || !k_tail || !block_tables || !context_lens || !out || !workspace) return PKV_EINVAL;
+  if (!al16(q) || !al16(cache) || !al16(k_tail) || !al16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PKV_EINVAL;
   if ((long long)max_blocks * block_size > 0x7fffffffLL) return PKV_ERANGE;
   const int G = n_h / n_kv;
@@ -799,10 +786,7 @@ static pkv_status decode_int4(const void* q, const uint8_t* k_codes, const void*
   a.err = err_flag;
   a.stages = vv->stages;
   a.window = window;
-  a.k_codes = k_codes;
-  a.v_codes = v_codes;
-  a.k_meta = static_cast<const __half*>(k_meta);
-  a.v_meta = static_cast<const __half*>(v_meta);
+  a.cache = cache;
   a.k_tail = static_cast<const __nv_bfloat16*>(k_tail);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = a.inline_plan ? cudaSuccess
@@ -819,27 +803,24 @@ static pkv_status decode_int4(const void* q, const uint8_t* k_codes, const void*
   return PKV_OK;
 }
 
-extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* k_codes, const void* k_meta,
-                                                 const uint8_t* v_codes, const void* v_meta, const void* k_tail,
+extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* cache, const void* k_tail,
                                                  const int32_t* block_tables, int max_blocks,
                                                  const int32_t* context_lens, float scale, int batch, int n_h,
                                                  int n_kv, int head_dim, int block_size, int num_blocks, void* out,
                                                  int out_dtype, void* workspace, size_t workspace_bytes,
                                                  int32_t* err_flag, void* stream) {
-  return decode_int4(q, k_codes, k_meta, v_codes, v_meta, k_tail, block_tables, max_blocks, context_lens, scale, 0,
+  return decode_int4(q, cache, k_tail, block_tables, max_blocks, context_lens, scale, 0,
                      batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace, workspace_bytes,
                      err_flag, stream);
 }
 
-extern "C" pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uint8_t* k_codes, const void* k_meta,
-                                                        const uint8_t* v_codes, const void* v_meta,
-                                                        const void* k_tail, const int32_t* block_tables,
+extern "C" pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uint8_t* cache, const void* k_tail,
+                                                        const int32_t* block_tables,
                                                         int max_blocks, const int32_t* context_lens, float scale,
                                                         int window, int batch, int n_h, int n_kv, int head_dim,
                                                         int block_size, int num_blocks, void* out, int out_dtype,
                                                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
                                                         void* stream) {
-  return decode_int4(q, k_codes, k_meta, v_codes, v_meta, k_tail, block_tables, max_blocks, context_lens, scale,
-                     window, batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace,
+  return decode_int4(q, cache, k_tail, block_tables, max_blocks, context_lens, scale, window, batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace,
                      workspace_bytes, err_flag, stream);
 }
