@@ -64,18 +64,27 @@ __global__ void __launch_bounds__(256) rope_shift_kernel(__nv_bfloat16* __restri
   }
   __syncthreads();
   const int rows = n_kv * block_size;
-  uint32_t* base = reinterpret_cast<uint32_t*>(k_pool + (size_t)phys * rows * D);
-  constexpr int PAIRS = H / 2;                                // bf16x2 words per half row
-  for (int idx = threadIdx.x; idx < rows * PAIRS; idx += blockDim.x) {
-    const int r = idx / PAIRS, w = idx - r * PAIRS;
-    uint32_t* row = base + (size_t)r * (D / 2);
-    const uint32_t a = row[w], b = row[w + PAIRS];
-    const int j = 2 * w;
-    const float x1a = bf16_lo(a), x1b = bf16_hi(a), x2a = bf16_lo(b), x2b = bf16_hi(b);
-    const float y1a = x1a * cs[j] - x2a * sn[j], y1b = x1b * cs[j + 1] - x2b * sn[j + 1];
-    const float y2a = x1a * sn[j] + x2a * cs[j], y2b = x1b * sn[j + 1] + x2b * cs[j + 1];
-    row[w] = pack_bf16(y1a, y1b);
-    row[w + PAIRS] = pack_bf16(y2a, y2b);
+  // one 16-byte vector of each half of a row per item: channels j0..j0+7 and their partners
+  constexpr int V = H / 8;                                    // vectors per half row
+  uint4* base = reinterpret_cast<uint4*>(k_pool + (size_t)phys * rows * D);
+  for (int idx = threadIdx.x; idx < rows * V; idx += blockDim.x) {
+    const int r = idx / V, v = idx - r * V;
+    uint4* row = base + (size_t)r * (D / 8);
+    uint4 a = row[v], b = row[v + V];
+    const int j0 = 8 * v;
+    auto rot = [&](uint32_t& wa, uint32_t& wb, int j) {     // channels j, j + 1 and j + H, j + H + 1
+      const float x1a = bf16_lo(wa), x1b = bf16_hi(wa), x2a = bf16_lo(wb), x2b = bf16_hi(wb);
+      const float y1a = x1a * cs[j] - x2a * sn[j], y1b = x1b * cs[j + 1] - x2b * sn[j + 1];
+      const float y2a = x1a * sn[j] + x2a * cs[j], y2b = x1b * sn[j + 1] + x2b * cs[j + 1];
+      wa = pack_bf16(y1a, y1b);
+      wb = pack_bf16(y2a, y2b);
+    };
+    rot(a.x, b.x, j0);
+    rot(a.y, b.y, j0 + 2);
+    rot(a.z, b.z, j0 + 4);
+    rot(a.w, b.w, j0 + 6);
+    row[v] = a;
+    row[v + V] = b;
   }
 }
 
@@ -123,12 +132,15 @@ extern "C" pkv_status pkv_rope_shift_k(void* k_pool, const int32_t* block_ids, c
   RopeFreq f = {};
   for (int j = 0; j < head_dim / 2; ++j) f.inv_freq[j] = std::pow(rope_base, -2.0 * j / head_dim);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // one thread per 16-byte vector pair of a block, at most 256 (they loop), at least 64
+  const long long items = (long long)n_kv * block_size * (head_dim / 16);
+  const int threads = items >= 256 ? 256 : (items <= 64 ? 64 : (int)((items + 31) / 32 * 32));
   if (head_dim == 128)
-    rope_shift_kernel<128><<<n_blocks, 256, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
-                                                     num_blocks, n_kv, block_size, f, err_flag);
+    rope_shift_kernel<128><<<n_blocks, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
+                                                         num_blocks, n_kv, block_size, f, err_flag);
   else
-    rope_shift_kernel<64><<<n_blocks, 256, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
-                                                    num_blocks, n_kv, block_size, f, err_flag);
+    rope_shift_kernel<64><<<n_blocks, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
+                                                        num_blocks, n_kv, block_size, f, err_flag);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
