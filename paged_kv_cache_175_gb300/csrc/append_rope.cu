@@ -12,6 +12,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         int vec_per_row, int n_kv, int block_size,
                                                         long long n_slots, uint4* __restrict__ k_pool,
                                                         uint4* __restrict__ v_pool, int32_t* err) {
+  grid_dep_launch();                       // the attention's setup may overlap this kernel
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const long long row = idx / vec_per_row;                  // (token, head)

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
     prefetch_tensormap(&tmv);
   }
   __syncthreads();
-  grid_dep_wait();                  // plan kernel's cum / ctx_eff are visible after this
+  if (!a.inline_plan) grid_dep_wait();   // the plan kernel's cum / ctx_eff / cursors
   grid_dep_launch();
 
   const int producer_warp = PW ? MT : 0;
@@ -88,6 +88,11 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
   const long long pstart = pi.pstart, pend = pi.pend;
   const int len = (int)(pend - pstart);
   if (len <= 0) return;
+  // The setup above reads only this call's inputs; the pools may still be being written by
+  // the kernel before this one on the stream (an append launched ahead of the attention),
+  // so every thread waits for it here, with the piece's first block-table line on its way.
+  if (warp == producer_warp && lane == 0) prefetch_l2(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + cur.blk);
+  if (a.inline_plan) grid_dep_wait();
 
   // ---------------- producer state (warp-uniform) ----------------
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
 // Phase 2: K rows of blocks that stay unfinished after this call go to the tail.
 template <int D>
 __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a) {
+  grid_dep_launch();                       // the attention's setup may overlap this kernel
   constexpr int VEC = D / 8;                                 // 16-byte vectors per row
   const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= (long long)a.n_tok * a.n_kv * VEC) return;
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
     fence_barrier_init();
   }
   __syncthreads();
-  grid_dep_wait();
+  if (!a.inline_plan) grid_dep_wait();   // the plan kernel's cum / ctx_eff / cursors
   grid_dep_launch();
 
   Cursor cur;
@@ -285,6 +286,11 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
   const long long pstart = pi.pstart, pend = pi.pend;
   const int len = (int)(pend - pstart);
   if (len <= 0) return;
+  // The setup above reads only this call's inputs; the cache and the K tail may still be
+  // being written by the kernel before this one on the stream (the quantize-on-append),
+  // so every thread waits for it here, with the piece's first block-table line on its way.
+  if (warp == 0 && lane == 0) prefetch_l2(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + cur.blk);
+  if (a.inline_plan) grid_dep_wait();
 
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
