@@ -63,8 +63,9 @@ struct QuantAppendArgs {
 
 // Phase 1: one warp per (token, kv head).  V is quantized per token; a token that fills
 // the last row of its block also quantizes that block's K per channel, taking rows
-// appended earlier in this call from `k` and older rows from the tail.
-template <int D>
+// appended earlier in this call from `k` and older rows from the tail (all BS rows of a
+// lane's channel are loaded before any is used).
+template <int D, int BS>
 __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs a) {
   constexpr int CPL = D / 32;                   // V channels per lane
   constexpr int LPW = 8 / CPL;                  // lanes per 32-bit code word
@@ -79,7 +80,6 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
     if (lane == 0 && g == 0) set_err(a.err, PKV_DEV_BAD_SLOT);
     return;
   }
-  const int BS = a.block_size;
   const long long blk = slot / BS;
   const int row = (int)(slot - blk * BS);
   const size_t tile = (size_t)blk * a.n_kv + g;           // (block, kv head)
@@ -144,21 +144,35 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
                                                    : krow_tail + (size_t)r * D;
       return __bfloat162float(p[c]);
     };
-    float lo = val(0), hi = lo;
-    for (int r = 1; r < BS; ++r) {
-      const float x = val(r);
-      lo = fminf(lo, x);
-      hi = fmaxf(hi, x);
+    // rows in chunks of 8, each chunk's loads issued before any is used
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll 1
+    for (int r0 = 0; r0 < BS; r0 += 8) {
+      float x[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) x[r] = val(r0 + r);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        lo = fminf(lo, x[r]);
+        hi = fmaxf(hi, x[r]);
+      }
     }
     const GroupQuant q = group_params(lo, hi);
     kmeta[c] = q.s16;
     kmeta[D + c] = q.m16;
-    for (int r = 0; r < BS; ++r) {
-      uint32_t word = quant_code(val(r), q) << (4 * nibble_of(c & 7));
-      word |= __shfl_xor_sync(FULL_MASK, word, 1);
-      word |= __shfl_xor_sync(FULL_MASK, word, 2);
-      word |= __shfl_xor_sync(FULL_MASK, word, 4);
-      if ((lane & 7) == 0) kcodes[(size_t)r * (D / 8) + c / 8] = word;
+#pragma unroll 1
+    for (int r0 = 0; r0 < BS; r0 += 8) {
+      float x[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) x[r] = val(r0 + r);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        uint32_t word = quant_code(x[r], q) << (4 * nibble_of(c & 7));
+        word |= __shfl_xor_sync(FULL_MASK, word, 1);
+        word |= __shfl_xor_sync(FULL_MASK, word, 2);
+        word |= __shfl_xor_sync(FULL_MASK, word, 4);
+        if ((lane & 7) == 0) kcodes[(size_t)(r0 + r) * (D / 8) + c / 8] = word;
+      }
     }
   }
 }
@@ -731,13 +745,12 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
   const unsigned g1 = (unsigned)((warps * 32 + 255) / 256);
   const long long vecs = warps * (head_dim / 8);
   const unsigned g2 = (unsigned)((vecs + 255) / 256);
-  if (head_dim == 128) {
-    quant_append_kernel<128><<<g1, 256, 0, st>>>(a);
-    tail_write_kernel<128><<<g2, 256, 0, st>>>(a);
-  } else {
-    quant_append_kernel<64><<<g1, 256, 0, st>>>(a);
-    tail_write_kernel<64><<<g2, 256, 0, st>>>(a);
-  }
+#define PKV_Q(d, b) \
+  if (head_dim == d && block_size == b) quant_append_kernel<d, b><<<g1, 256, 0, st>>>(a);
+  PKV_Q(128, 16) PKV_Q(128, 32) PKV_Q(128, 64) PKV_Q(64, 16) PKV_Q(64, 32) PKV_Q(64, 64)
+#undef PKV_Q
+  if (head_dim == 128) tail_write_kernel<128><<<g2, 256, 0, st>>>(a);
+  else tail_write_kernel<64><<<g2, 256, 0, st>>>(a);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
