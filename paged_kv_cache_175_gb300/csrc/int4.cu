@@ -255,15 +255,22 @@ __device__ __forceinline__ uint32_t mask_pair_h(uint32_t b, int t, int lead, int
   return b & ((t < ntok && t >= lead ? 0x0000ffffu : 0u) | (t + 1 < ntok && t + 1 >= lead ? 0xffff0000u : 0u));
 }
 
-template <int D, int BS>
+// TB cache records (blocks) per ring stage.
+template <int D, int BS, int TB>
 __host__ __device__ constexpr size_t int4_smem_bytes(int stages) {
-  return 128 + (size_t)stages * (Int4Tile<D, BS>::STAGE + 16 + 16);
+  return 128 + (size_t)stages * (TB * Int4Tile<D, BS>::STAGE + 16 + 16);
 }
 
-template <int D, int BS, int NH, int MT>
-__global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 : 0) decode_int4_kernel(const DecodeArgs a) {
+// TB = 2: a stage holds two consecutive blocks of one segment when the piece has them
+// (32 token rows per pass at block size 16: the per-stage loop, barrier, producer and
+// softmax work is shared by twice the tokens).
+template <int D, int BS, int NH, int MT, int TB>
+__global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 && NH == 1 ? 16 : 0))
+    decode_int4_kernel(const DecodeArgs a) {
   using T = Int4Tile<D, BS>;
-  constexpr int TT = BS / 16;       // 16-token tiles per block
+  constexpr int TPB = BS / 16;      // 16-token tiles per block
+  constexpr int TT = TB * TPB;      // 16-token tiles per stage
+  constexpr int SST = TB * T::STAGE;
   constexpr int KS = D / 16;        // k-steps of K Q^T
   constexpr int MD = D / 16;        // 16-channel m-tiles of O^T
   constexpr int HW = 8 * NH;        // heads per warp
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int S = a.stages;
-  int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * T::STAGE);
+  int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * SST);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + S);
   uint64_t* empty = full + S;
   __shared__ volatile int abort_flag;
@@ -308,17 +315,21 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
 
   int w_seq = -1, w_base = 0, w_phys = -1, n_seq = -1, n_base = 0, n_phys = -1;
   const uint64_t pol = policy_evict_first();
-  // ring position of the next issue / the next tile consumed (slot, and the parity of the
+  // ring position of the next issue / the next stage consumed (slot, and the parity of the
   // pass over the ring), advanced in order instead of dividing by the stage count
   int p_slot = 0, c_slot = 0;
   uint32_t p_phase = 0, c_phase = 0;
+  int pj = 0;                       // next block of the piece to issue (producer warp)
+  int issued = 0;                   // stages issued (producer warp)
 
   const uint32_t ring_sa = smem_u32(smem);                   // ring, then meta[S], then full[S]
   // constants of the segment the producer is in, set when it enters one: its last block,
   // and pack_rows(rows of the last block, rows of block 0 before the window, F_WHOLE)
   int seg_last = 0, seg_rows = 0;
 
-  auto issue = [&](int j) {
+  // Issues the stage starting at block pj: that block, and with TB = 2 the next one too
+  // when it is in the same segment and in the piece.
+  auto issue = [&]() {
     if (cur.s != w_seq || cur.blk < w_base || cur.blk >= w_base + 32) {
       if (cur.s == n_seq && cur.blk >= n_base && cur.blk < n_base + 32) {
         w_seq = n_seq; w_base = n_base; w_phys = n_phys;
@@ -333,13 +344,23 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
       n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
     }
     const int phys = __shfl_sync(FULL_MASK, w_phys, cur.blk - w_base);
+    const bool pair = TB == 2 && cur.blk + 1 < cur.nb && pj + 1 < len;
+    int phys1 = -1;
+    if (TB == 2) {
+      // the next block's entry is in this window or, past its end, in the prefetched one
+      // (which then starts at w_base + 32, as the block is in the segment)
+      const int b1 = cur.blk + 1;
+      const int x = __shfl_sync(FULL_MASK, w_phys, (b1 - w_base) & 31);
+      const int y = __shfl_sync(FULL_MASK, n_phys, (b1 - n_base) & 31);
+      phys1 = b1 < w_base + 32 ? x : y;
+    }
     const int slot = p_slot;
-    const uint32_t ph = p_phase;                               // parity of pass j / S
+    const uint32_t ph = p_phase;                               // parity of pass issued / S
     if (++p_slot == S) {
       p_slot = 0;
       p_phase ^= 1u;
     }
-    const bool first = j == 0 || cur.blk == 0;
+    const bool first = pj == 0 || cur.blk == 0;
     if (first) {
       seg_last = cur.nb - 1;
       seg_rows = pack_rows(cur.ctx - (cur.b0 + seg_last) * BS, window_lead(cur.ctx, a.window, BS),
@@ -356,15 +377,17 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
     // order of its generic-proxy reads before the async-proxy writes is needed.  Several
     // consumer warps release the slot through the empty barrier.
     bool ok_wait = true;
-    if (MT > 1 && j >= S) {
-      if (lane == 0) ok_wait = mbar_wait(&empty[slot], ph ^ 1u);   // released in pass j / S - 1
+    if (MT > 1 && issued >= S) {
+      if (lane == 0) ok_wait = mbar_wait(&empty[slot], ph ^ 1u);   // released in the previous pass
       ok_wait = __shfl_sync(FULL_MASK, ok_wait, 0);
     }
-    const bool last = cur.blk == seg_last;
-    const int ntok = last ? (seg_rows & 255) : BS;
-    const bool ok = (unsigned)phys < (unsigned)a.num_blocks, go = ok && ok_wait;
+    const int nblk = pair ? 2 : 1;
+    const bool last = cur.blk + nblk - 1 == seg_last;
+    const int ntok = (nblk - 1) * BS + (last ? (seg_rows & 255) : BS);   // rows of the stage
+    const bool ok = (unsigned)phys < (unsigned)a.num_blocks && (!pair || (unsigned)phys1 < (unsigned)a.num_blocks);
+    const bool go = ok && ok_wait, end = pj + nblk >= len;
     const int flags = (seg_rows >> 8 & F_WHOLE) | (ok ? F_VALID : 0) | (first ? F_FIRST : 0) |
-                      (last || j == len - 1 ? F_LAST : 0);
+                      (last || end ? F_LAST : 0) | (pair ? F_PAIR : 0) | (end ? F_END : 0);
     if (lane == 0) {
       if (!ok_wait) {
         set_err(a.err, PKV_DEV_TIMEOUT);
@@ -373,17 +396,25 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
       if (!ok) set_err(a.err, PKV_DEV_BAD_BLOCK);
       meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, cur.blk == 0 ? seg_rows >> 16 : 0, flags));
       if (go) {
-        // the whole record, also for the unfinished block (its K codes are then unused)
-        mbar_arrive_expect_tx(&full[slot], T::REC);
-        if (MT == 1 && j >= S) fence_proxy_async_smem();
-        bulk_g2s_u32(ring_sa + (uint32_t)slot * T::STAGE,
-                     a.cache + ((size_t)(unsigned)phys * (unsigned)a.n_kv + (unsigned)cur.g) * T::REC, T::REC,
-                     ring_sa + S * (T::STAGE + 16) + 8u * (uint32_t)slot, pol);
+        // whole records, also for the unfinished block (its K codes are then unused)
+        const uint32_t bar = ring_sa + S * (SST + 16) + 8u * (uint32_t)slot;
+        const uint32_t dst = ring_sa + (uint32_t)slot * SST;
+        mbar_arrive_expect_tx(&full[slot], nblk * T::REC);
+        if (MT == 1 && issued >= S) fence_proxy_async_smem();
+        bulk_g2s_u32(dst, a.cache + ((size_t)(unsigned)phys * (unsigned)a.n_kv + (unsigned)cur.g) * T::REC, T::REC,
+                     bar, pol);
+        if (pair)
+          bulk_g2s_u32(dst + T::STAGE,
+                       a.cache + ((size_t)(unsigned)phys1 * (unsigned)a.n_kv + (unsigned)cur.g) * T::REC, T::REC,
+                       bar, pol);
       } else {
         mbar_arrive(&full[slot]);
       }
     }
-    if (j + 1 < len) cursor_next(cur, a);
+    if (pair) ++cur.blk;                                       // the second block, same segment
+    pj += nblk;
+    ++issued;
+    if (pj < len) cursor_next(cur, a);
   };
 
   // ---------------- consumer state (warp w: local heads [w*HW, (w+1)*HW)) ----------------
@@ -401,21 +432,20 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
   const int cb = tig * CB;           // first K channel of this thread
   const int cv = gid * CV;           // first V channel of this thread
 
-  if (warp == 0) {
-    const int pre = len < S ? len : S;
-    for (int j = 0; j < pre; ++j) issue(j);
-  }
+  if (warp == 0)
+    for (int k = 0; k < S && pj < len; ++k) issue();
 
-  int consumed = 0;
-  for (int j = 0; j < len; ++j) {
+  int consumed = 0;                  // stages consumed
+  for (;;) {
     const int slot = c_slot;
     if (!mbar_wait(&full[slot], c_phase) || abort_flag) {
       set_err(a.err, PKV_DEV_TIMEOUT);
       abort_flag = 1;
       break;
     }
-    consumed = j + 1;
+    ++consumed;
     const int4 mt = meta[slot];
+    // ntok, lead: the stage's attended rows are [lead, ntok) of its TT * 16
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;
 
@@ -439,9 +469,12 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
     }
 
     if (flags & F_VALID) {
-      const uint8_t* st = smem + (size_t)slot * T::STAGE;
-      const bool partial = ntok < BS;                            // the unfinished block: K from the tail
-      const bool masked = partial || lead > 0;
+      const uint8_t* stg = smem + (size_t)slot * SST;
+      const int nblk = TB > 1 && (flags & F_PAIR) ? 2 : 1;      // records in the stage
+      // the stage's last record is the sequence's unfinished block (K from the tail) when
+      // its rows stop short of the block
+      const int tail_rec = ntok < nblk * BS ? nblk - 1 : -1;   // (at most one record per stage)
+      const bool masked = ntok < TT * 16 || lead > 0;
       // ---- S^T = K^ Q^T (fp16 in, fp32 accumulate; even / odd k-steps in two accumulators) ----
       float sc[TT][NH][4], sx[TT][NH][4];
 #pragma unroll
@@ -450,71 +483,78 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
           for (int i = 0; i < 4; ++i) sc[t][nh][i] = sx[t][nh][i] = 0.f;
-      if (!partial) {
-        uint32_t s2[CB / 2], m2[CB / 2];                          // (s, m) of channel pairs cb + 2k
-        const uint4* kms = reinterpret_cast<const uint4*>(st + T::KM + cb * 2);
-        const uint4* kmm = reinterpret_cast<const uint4*>(st + T::KM + 2 * D + cb * 2);
 #pragma unroll
-        for (int k4 = 0; k4 < CB / 8; ++k4) {
-          const uint4 a4 = kms[k4], b4 = kmm[k4];
-          s2[4 * k4] = a4.x; s2[4 * k4 + 1] = a4.y; s2[4 * k4 + 2] = a4.z; s2[4 * k4 + 3] = a4.w;
-          m2[4 * k4] = b4.x; m2[4 * k4 + 1] = b4.y; m2[4 * k4 + 2] = b4.z; m2[4 * k4 + 3] = b4.w;
-        }
-#pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          uint32_t w0[KW], w1[KW];                                // code words of rows gid, gid+8
-          const uint8_t* r0 = st + T::KC + (t * 16 + gid) * (D / 2) + tig * (D / 8);
-          const uint8_t* r1 = r0 + 8 * (D / 2);
-          if constexpr (KW == 4) {
-            const uint4 x = *reinterpret_cast<const uint4*>(r0), y = *reinterpret_cast<const uint4*>(r1);
-            w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
-            w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
-          } else {
-            const uint2 x = *reinterpret_cast<const uint2*>(r0), y = *reinterpret_cast<const uint2*>(r1);
-            w0[0] = x.x; w0[1] = x.y;
-            w1[0] = y.x; w1[1] = y.y;
-          }
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const int w = ks >> 1, hs = 2 * (ks & 1), pr = 4 * w + hs;
-            uint32_t ka[4];
-            ka[0] = dq2(lop_nib(w0[w] >> (4 * hs)), s2[pr], m2[pr]);
-            ka[1] = dq2(lop_nib(w1[w] >> (4 * hs)), s2[pr], m2[pr]);
-            ka[2] = dq2(lop_nib(w0[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
-            ka[3] = dq2(lop_nib(w1[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
-#pragma unroll
-            for (int nh = 0; nh < NH; ++nh) {
-              if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
-              else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
-            }
-          }
-        }
-      } else {
-        // unfinished block: K rows from the bf16 tail in global memory (prefetched to L2)
-        const uint4* tl = reinterpret_cast<const uint4*>(a.k_tail + ((size_t)s * a.n_kv + g) * BS * D);
-#pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          uint32_t w0[CB / 2], w1[CB / 2];                        // bf16 pairs of channels cb + 2k
-          const uint4* r0 = tl + ((size_t)(t * 16 + gid) * D + cb) / 8;
-          const uint4* r1 = r0 + D;                               // 8 rows further (D / 8 uint4 per row)
+      for (int rec = 0; rec < TB; ++rec) {
+        if (rec >= nblk) continue;
+        const uint8_t* st = stg + rec * T::STAGE;
+        if (rec != tail_rec) {
+          uint32_t s2[CB / 2], m2[CB / 2];                        // (s, m) of channel pairs cb + 2k
+          const uint4* kms = reinterpret_cast<const uint4*>(st + T::KM + cb * 2);
+          const uint4* kmm = reinterpret_cast<const uint4*>(st + T::KM + 2 * D + cb * 2);
 #pragma unroll
           for (int k4 = 0; k4 < CB / 8; ++k4) {
-            const uint4 x = __ldg(r0 + k4), y = __ldg(r1 + k4);
-            w0[4 * k4] = x.x; w0[4 * k4 + 1] = x.y; w0[4 * k4 + 2] = x.z; w0[4 * k4 + 3] = x.w;
-            w1[4 * k4] = y.x; w1[4 * k4 + 1] = y.y; w1[4 * k4 + 2] = y.z; w1[4 * k4 + 3] = y.w;
+            const uint4 a4 = kms[k4], b4 = kmm[k4];
+            s2[4 * k4] = a4.x; s2[4 * k4 + 1] = a4.y; s2[4 * k4 + 2] = a4.z; s2[4 * k4 + 3] = a4.w;
+            m2[4 * k4] = b4.x; m2[4 * k4 + 1] = b4.y; m2[4 * k4 + 2] = b4.z; m2[4 * k4 + 3] = b4.w;
           }
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            const int pr = 4 * (ks >> 1) + 2 * (ks & 1);
-            uint32_t ka[4];
-            ka[0] = bf2_to_h2(w0[pr]);
-            ka[1] = bf2_to_h2(w1[pr]);
-            ka[2] = bf2_to_h2(w0[pr + 1]);
-            ka[3] = bf2_to_h2(w1[pr + 1]);
+          for (int tt = 0; tt < TPB; ++tt) {
+            const int t = rec * TPB + tt;
+            uint32_t w0[KW], w1[KW];                              // code words of rows gid, gid+8
+            const uint8_t* q0 = st + T::KC + (tt * 16 + gid) * (D / 2) + tig * (D / 8);
+            const uint8_t* q1 = q0 + 8 * (D / 2);
+            if constexpr (KW == 4) {
+              const uint4 x = *reinterpret_cast<const uint4*>(q0), y = *reinterpret_cast<const uint4*>(q1);
+              w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
+              w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
+            } else {
+              const uint2 x = *reinterpret_cast<const uint2*>(q0), y = *reinterpret_cast<const uint2*>(q1);
+              w0[0] = x.x; w0[1] = x.y;
+              w1[0] = y.x; w1[1] = y.y;
+            }
 #pragma unroll
-            for (int nh = 0; nh < NH; ++nh) {
-              if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
-              else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+            for (int ks = 0; ks < KS; ++ks) {
+              const int w = ks >> 1, hs = 2 * (ks & 1), pr = 4 * w + hs;
+              uint32_t ka[4];
+              ka[0] = dq2(lop_nib(w0[w] >> (4 * hs)), s2[pr], m2[pr]);
+              ka[1] = dq2(lop_nib(w1[w] >> (4 * hs)), s2[pr], m2[pr]);
+              ka[2] = dq2(lop_nib(w0[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
+              ka[3] = dq2(lop_nib(w1[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
+#pragma unroll
+              for (int nh = 0; nh < NH; ++nh) {
+                if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+                else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+              }
+            }
+          }
+        } else {
+          // unfinished block: K rows from the bf16 tail in global memory (prefetched to L2)
+          const uint4* tl = reinterpret_cast<const uint4*>(a.k_tail + ((size_t)s * a.n_kv + g) * BS * D);
+#pragma unroll
+          for (int tt = 0; tt < TPB; ++tt) {
+            const int t = rec * TPB + tt;
+            uint32_t w0[CB / 2], w1[CB / 2];                      // bf16 pairs of channels cb + 2k
+            const uint4* q0 = tl + ((size_t)(tt * 16 + gid) * D + cb) / 8;
+            const uint4* q1 = q0 + D;                             // 8 rows further (D / 8 uint4 per row)
+#pragma unroll
+            for (int k4 = 0; k4 < CB / 8; ++k4) {
+              const uint4 x = __ldg(q0 + k4), y = __ldg(q1 + k4);
+              w0[4 * k4] = x.x; w0[4 * k4 + 1] = x.y; w0[4 * k4 + 2] = x.z; w0[4 * k4 + 3] = x.w;
+              w1[4 * k4] = y.x; w1[4 * k4 + 1] = y.y; w1[4 * k4 + 2] = y.z; w1[4 * k4 + 3] = y.w;
+            }
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              const int pr = 4 * (ks >> 1) + 2 * (ks & 1);
+              uint32_t ka[4];
+              ka[0] = bf2_to_h2(w0[pr]);
+              ka[1] = bf2_to_h2(w1[pr]);
+              ka[2] = bf2_to_h2(w0[pr + 1]);
+              ka[3] = bf2_to_h2(w1[pr + 1]);
+#pragma unroll
+              for (int nh = 0; nh < NH; ++nh) {
+                if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+                else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+              }
             }
           }
         }
@@ -527,9 +567,12 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
           for (int i = 0; i < 4; ++i) sc[t][nh][i] += sx[t][nh][i];
       softmax_tile<TT, NH, MD>(sc, m, l, o, gid, ntok, lead, a.scale_log2);
       // ---- O^T += V^T P^T (fp16, P as high + low) ----
-      const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + T::VM);
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
+        const int rec = t / TPB, r0 = (t % TPB) * 16;             // record, first row in it
+        if (rec >= nblk) continue;
+        const uint8_t* st = stg + rec * T::STAGE;
+        const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + T::VM);
         uint32_t bh[NH][2], bl[NH][2];
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
@@ -542,16 +585,17 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
             bh[nh][r] = movmatrix_t(hi);
             bl[nh][r] = movmatrix_t(lo);
           }
-        const int t0 = t * 16 + 2 * tig;                         // a0/a1: tokens t0, t0+1; a2/a3: +8
+        const int t0 = r0 + 2 * tig;                 // a0/a1: record rows t0, t0+1; a2/a3: +8
+        const int u0 = t * 16 + 2 * tig;             // the same rows counted in the stage
         uint32_t sA = prmt(vm[t0], vm[t0 + 1], 0x5410), mA = prmt(vm[t0], vm[t0 + 1], 0x7632);
         uint32_t sB = prmt(vm[t0 + 8], vm[t0 + 9], 0x5410), mB = prmt(vm[t0 + 8], vm[t0 + 9], 0x7632);
         if (masked) {
           // rows outside [lead, ntok) get scale = min = 0, so their V^ is exactly 0 whatever
           // their codes (rows past ntok were never written)
-          sA = mask_pair_h(sA, t0, lead, ntok);
-          mA = mask_pair_h(mA, t0, lead, ntok);
-          sB = mask_pair_h(sB, t0 + 8, lead, ntok);
-          mB = mask_pair_h(mB, t0 + 8, lead, ntok);
+          sA = mask_pair_h(sA, u0, lead, ntok);
+          mA = mask_pair_h(mA, u0, lead, ntok);
+          sB = mask_pair_h(sB, u0 + 8, lead, ntok);
+          mB = mask_pair_h(mB, u0 + 8, lead, ntok);
         }
         const uint8_t* vc = st + T::VC + cv / 2;
 #pragma unroll
@@ -631,15 +675,16 @@ __global__ void __launch_bounds__(MT * 32, BS == 16 && MT == 1 && NH == 1 ? 16 :
 
     __syncwarp();
     if (MT > 1 && lane == 0) mbar_arrive(&empty[slot]);
-    if (warp == 0 && j + S < len) issue(j + S);
+    if (warp == 0 && pj < len) issue();
     if (++c_slot == S) {
       c_slot = 0;
       c_phase ^= 1u;
     }
+    if (flags & F_END) break;
   }
 
   if (abort_flag && threadIdx.x == 0) {
-    const int issued = len < consumed + S ? len : consumed + S;
+    // let the copies of the stages issued but not consumed land before the CTA exits
     for (int j = consumed; j < issued; ++j)
       if (!mbar_wait(&full[j % S], (j / S) & 1)) break;
   }
@@ -654,12 +699,12 @@ struct Int4Variant {
   int P;
 };
 
-template <int D, int BS, int NH, int MT>
+template <int D, int BS, int NH, int MT, int TB>
 static Int4Variant make_int4_variant() {
   Int4Variant v;
-  v.fn = (const void*)decode_int4_kernel<D, BS, NH, MT>;
-  v.stages = ring_stages(Int4Tile<D, BS>::STAGE, BS == 16 ? 11264 : 16384, "PKV_STAGES_INT4");
-  v.smem = int4_smem_bytes<D, BS>(v.stages);
+  v.fn = (const void*)decode_int4_kernel<D, BS, NH, MT, TB>;
+  v.stages = ring_stages(TB * Int4Tile<D, BS>::STAGE, BS == 16 ? 11264 : 16384, "PKV_STAGES_INT4");
+  v.smem = int4_smem_bytes<D, BS, TB>(v.stages);
   v.warps = MT;
   v.P = 0;
   return v;
@@ -675,10 +720,10 @@ static Int4Variant* lookup_int4(int D, int BS, int tiling) {
   if (!ready[di][bi][ti]) {
 #define PKV_V(d, b)                                               \
   if (D == d && BS == b) {                                        \
-    if (ti == 0) v = make_int4_variant<d, b, 1, 1>();             \
-    else if (ti == 1) v = make_int4_variant<d, b, 2, 1>();        \
-    else if (ti == 2) v = make_int4_variant<d, b, 2, 2>();        \
-    else v = make_int4_variant<d, b, 2, 4>();                     \
+    if (ti == 0) v = make_int4_variant<d, b, 1, 1, b == 16 ? 2 : 1>(); \
+    else if (ti == 1) v = make_int4_variant<d, b, 2, 1, 1>();     \
+    else if (ti == 2) v = make_int4_variant<d, b, 2, 2, 1>();     \
+    else v = make_int4_variant<d, b, 2, 4, 1>();                  \
   }
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
