@@ -31,9 +31,10 @@ struct Bf16Tile {
   static constexpr int STAGE = 2 * TILE;
 };
 
-template <int D, int BS>
+// TB blocks (K and V tiles each) per ring stage.
+template <int D, int BS, int TB>
 __host__ __device__ constexpr size_t bf16_smem_bytes(int stages) {
-  return 1024 + (size_t)stages * (Bf16Tile<D, BS>::STAGE + 16 + 16);
+  return 1024 + (size_t)stages * (TB * Bf16Tile<D, BS>::STAGE + 16 + 16);
 }
 
 // Keep the halves of a pair of rows (t, t + 1) that lie in [lead, ntok); zero the others.
@@ -46,20 +47,25 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t b, int t, int lead, int n
 // dedicated warp takes the block-table walk, the barrier bookkeeping and the copy issue
 // (about as many cycles per tile as the tile's arithmetic) off the consumers' path; it
 // costs one warp of registers, so it is used where the consumers are light (one warp).
-template <int D, int BS, int NH, int MT, bool PW>
+// TB = 2: a stage holds two consecutive blocks of one segment when the piece has them, so
+// each pass covers 32 token rows at block size 16 (used for groups of 17-32 heads, whose
+// consumers spend the most per pass).
+template <int D, int BS, int NH, int MT, bool PW, int TB>
 __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
                                   (PW && BS <= 32) ? (NH == 1 ? 65536 / ((MT + 1) * 32 * 128) : 4) : 0)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const DecodeArgs a) {
   using T = Bf16Tile<D, BS>;
-  constexpr int TT = BS / 16;       // 16-token tiles per block
+  constexpr int TPB = BS / 16;      // 16-token tiles per block
+  constexpr int TT = TB * TPB;      // 16-token tiles per stage
+  constexpr int SST = TB * T::STAGE;
   constexpr int KS = D / 16;        // k-steps of K Q^T
   constexpr int MD = D / 16;        // 16-channel m-tiles of O^T
   constexpr int HW = 8 * NH;        // heads per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
-  int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * T::STAGE);
+  int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * SST);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + S);
   uint64_t* empty = full + S;
   __shared__ volatile int abort_flag;
@@ -102,7 +108,12 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
   int p_slot = 0, c_slot = 0;
   uint32_t p_phase = 0, c_phase = 0;
 
-  auto issue = [&](int j) {
+  int pj = 0;                       // next block of the piece to issue (producer warp)
+  int issued = 0;                   // stages issued (producer warp)
+
+  // Issues the stage starting at block pj: that block, and with TB = 2 the next one too
+  // when it is in the same segment and in the piece.
+  auto issue = [&]() {
     if (cur.s != w_seq || cur.blk < w_base || cur.blk >= w_base + 32) {
       if (cur.s == n_seq && cur.blk >= n_base && cur.blk < n_base + 32) {
         w_seq = n_seq; w_base = n_base; w_phys = n_phys;
@@ -117,35 +128,58 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
       n_phys = b < cur.nb ? __ldg(a.bt + (size_t)cur.s * a.max_blocks + cur.b0 + b) : -1;
     }
     const int phys = __shfl_sync(FULL_MASK, w_phys, cur.blk - w_base);
+    const bool pair = TB == 2 && cur.blk + 1 < cur.nb && pj + 1 < len;
+    int phys1 = -1;
+    if (TB == 2) {
+      // the next block's entry is in this window or, past its end, in the prefetched one
+      // (which then starts at w_base + 32, as the block is in the segment)
+      const int b1 = cur.blk + 1;
+      const int x = __shfl_sync(FULL_MASK, w_phys, (b1 - w_base) & 31);
+      const int y = __shfl_sync(FULL_MASK, n_phys, (b1 - n_base) & 31);
+      phys1 = b1 < w_base + 32 ? x : y;
+    }
     const int slot = p_slot;
-    const uint32_t ph = p_phase;                               // parity of pass j / S
+    const uint32_t ph = p_phase;                               // parity of pass issued / S
     if (++p_slot == S) {
       p_slot = 0;
       p_phase ^= 1u;
     }
     if (lane == 0) {
       bool ok_wait = true;
-      if (j >= S) ok_wait = mbar_wait(&empty[slot], ph ^ 1u);   // released in pass j / S - 1
+      if (issued >= S) ok_wait = mbar_wait(&empty[slot], ph ^ 1u);   // released in the previous pass
       if (!ok_wait) {
         set_err(a.err, PKV_DEV_TIMEOUT);
         abort_flag = 1;
       }
-      const int ntok = cur.blk == cur.nb - 1 ? cur.ctx - (cur.b0 + cur.blk) * BS : BS;
+      const int nblk = pair ? 2 : 1;
+      const int lb = cur.blk + nblk - 1;                       // the stage's last block
+      const int ntok = (nblk - 1) * BS + (lb == cur.nb - 1 ? cur.ctx - (cur.b0 + lb) * BS : BS);
       const int lead = cur.blk == 0 ? window_lead(cur.ctx, a.window, BS) : 0;
+      const bool end = pj + nblk >= len;
       int flags = 0;
-      if (j == 0 || cur.blk == 0) flags |= F_FIRST;
-      if (j == len - 1 || cur.blk == cur.nb - 1) flags |= F_LAST;
+      if (pj == 0 || cur.blk == 0) flags |= F_FIRST;
+      if (end || lb == cur.nb - 1) flags |= F_LAST;
       if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
-      const bool ok = (unsigned)phys < (unsigned)a.num_blocks;
+      if (pair) flags |= F_PAIR;
+      if (end) flags |= F_END;
+      const bool ok = (unsigned)phys < (unsigned)a.num_blocks && (!pair || (unsigned)phys1 < (unsigned)a.num_blocks);
       if (ok) flags |= F_VALID; else set_err(a.err, PKV_DEV_BAD_BLOCK);
       meta[slot] = make_int4(cur.s, cur.g, cur.blk, pack_rows(ntok, lead, flags));
       if (ok && ok_wait) {
-        mbar_arrive_expect_tx(&full[slot], T::STAGE);
-        uint8_t* st = smem + (size_t)slot * T::STAGE;
+        mbar_arrive_expect_tx(&full[slot], nblk * T::STAGE);
+        uint8_t* st = smem + (size_t)slot * SST;
 #pragma unroll
         for (int b = 0; b < T::NBOX; ++b) {
           tma_load_3d(st + b * T::BOX_BYTES, &tmk, b * 64, cur.g * BS, phys, &full[slot], pol);
           tma_load_3d(st + T::TILE + b * T::BOX_BYTES, &tmv, b * 64, cur.g * BS, phys, &full[slot], pol);
+        }
+        if (pair) {
+#pragma unroll
+          for (int b = 0; b < T::NBOX; ++b) {
+            tma_load_3d(st + T::STAGE + b * T::BOX_BYTES, &tmk, b * 64, cur.g * BS, phys1, &full[slot], pol);
+            tma_load_3d(st + T::STAGE + T::TILE + b * T::BOX_BYTES, &tmv, b * 64, cur.g * BS, phys1, &full[slot],
+                        pol);
+          }
         }
       } else {
         mbar_arrive(&full[slot]);
@@ -155,7 +189,10 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
         for (int off = 0; off < a.G * D * 2; off += 128) prefetch_l2(qp + off);
       }
     }
-    if (j + 1 < len) cursor_next(cur, a);
+    if (pair) ++cur.blk;                                       // the second block, same segment
+    pj += pair ? 2 : 1;
+    ++issued;
+    if (pj < len) cursor_next(cur, a);
   };
 
   // ---------------- consumer state (warp w: local heads [w*HW, (w+1)*HW)) ----------------
@@ -169,32 +206,29 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
   const int hw0 = warp * HW;                    // first local head of this warp
 
   if (PW && warp == MT) {
-    int j = 0;
-    for (; j < len && !abort_flag; ++j) issue(j);
+    while (pj < len && !abort_flag) issue();
     if (abort_flag && lane == 0) {
       // let the copies still in flight land before the CTA exits: wait (bounded) for the
-      // last tile issued on each slot
-      for (int k = 0; k < S && k < j; ++k) {
-        const int last = k + ((j - 1 - k) / S) * S;
+      // last stage issued on each slot
+      for (int k = 0; k < S && k < issued; ++k) {
+        const int last = k + ((issued - 1 - k) / S) * S;
         if (!mbar_wait(&full[k], (last / S) & 1)) break;
       }
     }
     return;
   }
-  if (!PW && warp == 0) {
-    const int pre = len < S ? len : S;
-    for (int j = 0; j < pre; ++j) issue(j);
-  }
+  if (!PW && warp == 0)
+    for (int k = 0; k < S && pj < len; ++k) issue();
 
-  int consumed = 0;
-  for (int j = 0; j < len; ++j) {
+  int consumed = 0;                  // stages consumed
+  for (;;) {
     const int slot = c_slot;
     if (!mbar_wait(&full[slot], c_phase) || abort_flag) {
       set_err(a.err, PKV_DEV_TIMEOUT);
       abort_flag = 1;
       break;
     }
-    consumed = j + 1;
+    ++consumed;
     const int4 mt = meta[slot];
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;   // first q head of the group
@@ -218,7 +252,8 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
     }
 
     if (flags & F_VALID) {
-      const uint32_t kb = smem_u32(smem + (size_t)slot * T::STAGE), vb = kb + T::TILE;
+      const uint32_t kb0 = smem_u32(smem + (size_t)slot * SST);   // block k: K at k * STAGE, V after it
+      const int nblk = TB > 1 && (flags & F_PAIR) ? 2 : 1;
       // ---- S^T = K Q^T: per 16-token tile and head n-tile, two accumulators (even / odd
       // k-steps) so the dependent mma chains are half as long ----
       float sc[TT][NH][4];
@@ -234,8 +269,10 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
         for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
           for (int t = 0; t < TT; ++t) {
+            if (t / TPB >= nblk) continue;
+            const uint32_t kb = kb0 + (t / TPB) * T::STAGE;
             const int mi = lane >> 3;
-            const int tok = t * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int tok = (t % TPB) * 16 + ((mi & 1) << 3) + (lane & 7);
             const int ch = 2 * ks + (mi >> 1);
             const uint32_t addr = kb + (ch >> 3) * T::BOX_BYTES + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
             uint32_t ka[4];
@@ -256,9 +293,11 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
       }
       softmax_tile<TT, NH, MD>(sc, m, l, o, gid, ntok, lead, a.scale_log2);
       // ---- O^T += V^T P^T, P as bf16 high + low ----
-      const bool partial = ntok < BS || lead > 0;
+      const bool partial = ntok < TT * 16 || lead > 0;
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
+        if (t / TPB >= nblk) continue;
+        const uint32_t vb = kb0 + (t / TPB) * T::STAGE + T::TILE;
         // B fragments of P^T (k = token, n = head): the S^T rows of tokens 0-7 / 8-15 of
         // the tile, packed per head pair and transposed
         uint32_t bh[NH][2], bl[NH][2];
@@ -276,7 +315,7 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
 #pragma unroll
         for (int md = 0; md < MD; ++md) {
           const int mi = lane >> 3;
-          const int tok = t * 16 + ((mi >> 1) << 3) + (lane & 7);
+          const int tok = (t % TPB) * 16 + ((mi >> 1) << 3) + (lane & 7);
           const int ch = 2 * md + (mi & 1);
           const uint32_t addr = vb + (ch >> 3) * T::BOX_BYTES + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4);
           uint32_t va[4];
@@ -349,17 +388,17 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
 
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    if (!PW && warp == 0 && j + S < len) issue(j + S);
+    if (!PW && warp == 0 && pj < len) issue();
     if (++c_slot == S) {
       c_slot = 0;
       c_phase ^= 1u;
     }
+    if (flags & F_END) break;
   }
 
   // After a timeout: let this CTA's copies already in flight land before exiting
   // (each wait is bounded, and the drain as a whole gives up at the first failure).
   if (!PW && abort_flag && threadIdx.x == 0) {
-    const int issued = len < consumed + S ? len : consumed + S;
     for (int j = consumed; j < issued; ++j)
       if (!mbar_wait(&full[j % S], (j / S) & 1)) break;
   }
@@ -375,15 +414,15 @@ struct Bf16Variant {
   int P;        // persistent CTAs on this device
 };
 
-template <int D, int BS, int NH, int MT, bool PW>
+template <int D, int BS, int NH, int MT, bool PW, int TB>
 static Bf16Variant make_variant() {
   Bf16Variant v;
-  v.fn = (const void*)decode_bf16_kernel<D, BS, NH, MT, PW>;
-  v.stage_bytes = Bf16Tile<D, BS>::STAGE;
+  v.fn = (const void*)decode_bf16_kernel<D, BS, NH, MT, PW, TB>;
+  v.stage_bytes = TB * Bf16Tile<D, BS>::STAGE;
   // measured best: 16 KB of ring per CTA with the dedicated producer (its consumer keeps
   // up, and more resident CTAs beat deeper prefetch), 24 KB with the inline one
   v.stages = ring_stages(v.stage_bytes, PW ? 16384 : 24576, "PKV_STAGES_BF16");
-  v.smem = bf16_smem_bytes<D, BS>(v.stages);
+  v.smem = bf16_smem_bytes<D, BS, TB>(v.stages);
   v.warps = MT + (PW ? 1 : 0);
   v.P = 0;
   return v;
@@ -400,10 +439,10 @@ static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   if (!ready[di][bi][ti]) {
 #define PKV_V(d, b)                                               \
   if (D == d && BS == b) {                                        \
-    if (ti == 0) v = make_variant<d, b, 1, 1, true>();            \
-    else if (ti == 1) v = make_variant<d, b, 1, 2, true>();       \
-    else if (ti == 2) v = make_variant<d, b, 2, 2, true>();       \
-    else v = make_variant<d, b, 2, 4, false>();                   \
+    if (ti == 0) v = make_variant<d, b, 1, 1, true, 1>();         \
+    else if (ti == 1) v = make_variant<d, b, 1, 2, true, 1>();    \
+    else if (ti == 2) v = make_variant<d, b, 2, 2, true, b == 16 ? 2 : 1>(); \
+    else v = make_variant<d, b, 2, 4, false, 1>();                \
   }
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
