@@ -63,8 +63,7 @@ struct QuantAppendArgs {
 
 // Phase 1: one warp per (token, kv head).  V is quantized per token; a token that fills
 // the last row of its block also quantizes that block's K per channel, taking rows
-// appended earlier in this call from `k` and older rows from the tail (all BS rows of a
-// lane's channel are loaded before any is used).
+// appended earlier in this call from `k` and older rows from the tail.
 template <int D, int BS>
 __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs a) {
   constexpr int CPL = D / 32;                   // V channels per lane
@@ -136,43 +135,82 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
   const __nv_bfloat16* krow_tail = a.k_tail + ((size_t)seq * a.n_kv + g) * BS * D;
   __half* kmeta = reinterpret_cast<__half*>(rec + (size_t)BS * D);
   uint32_t* kcodes = reinterpret_cast<uint32_t*>(rec);
-#pragma unroll 1
-  for (int cm = 0; cm < CPL; ++cm) {
-    const int c = lane + 32 * cm;                            // this lane's channel
-    auto val = [&](int r) -> float {
-      const __nv_bfloat16* p = r >= first_call_row ? krow_call + (size_t)(i - (BS - 1 - r)) * a.n_kv * D
-                                                   : krow_tail + (size_t)r * D;
-      return __bfloat162float(p[c]);
-    };
-    // rows in chunks of 8, each chunk's loads issued before any is used
-    float lo = INFINITY, hi = -INFINITY;
-#pragma unroll 1
-    for (int r0 = 0; r0 < BS; r0 += 8) {
-      float x[8];
+  // Lane (octet, row group): channels [8 octet, 8 octet + 8) -- one code word per row -- of
+  // the rows r0 + rg + RG k of each chunk of KR rows, loaded as 16-byte vectors, every load
+  // of a chunk issued before any is used.  The channel range comes from a min / max over the
+  // lane's rows and then across the row groups; a block of KR rows stays in registers from
+  // the range pass to the code pass.
+  constexpr int OCT = D / 8;                                 // channel octets
+  constexpr int RG = 32 / OCT;                               // row groups
+  constexpr int KR = 16;                                     // rows per chunk
+  constexpr int RPL = KR / RG;                               // rows per lane and chunk
+  const int oct = lane % OCT, rg = lane / OCT;
+  auto row_ptr = [&](int r) -> const __nv_bfloat16* {
+    return r >= first_call_row ? krow_call + (size_t)(i - (BS - 1 - r)) * a.n_kv * D : krow_tail + (size_t)r * D;
+  };
+  float x[RPL][8];
+  auto load_chunk = [&](int r0) {
+    uint4 v[RPL];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) x[r] = val(r0 + r);
+    for (int k = 0; k < RPL; ++k) v[k] = *reinterpret_cast<const uint4*>(row_ptr(r0 + rg + RG * k) + 8 * oct);
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        lo = fminf(lo, x[r]);
-        hi = fmaxf(hi, x[r]);
+    for (int k = 0; k < RPL; ++k) {
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[k][2 * e] = bf16_lo(w[e]);
+        x[k][2 * e + 1] = bf16_hi(w[e]);
       }
     }
-    const GroupQuant q = group_params(lo, hi);
-    kmeta[c] = q.s16;
-    kmeta[D + c] = q.m16;
+  };
+  float lo[8], hi[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    lo[c] = INFINITY;
+    hi[c] = -INFINITY;
+  }
 #pragma unroll 1
-    for (int r0 = 0; r0 < BS; r0 += 8) {
-      float x[8];
+  for (int r0 = 0; r0 < BS; r0 += KR) {
+    load_chunk(r0);
 #pragma unroll
-      for (int r = 0; r < 8; ++r) x[r] = val(r0 + r);
+    for (int k = 0; k < RPL; ++k)
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        uint32_t word = quant_code(x[r], q) << (4 * nibble_of(c & 7));
-        word |= __shfl_xor_sync(FULL_MASK, word, 1);
-        word |= __shfl_xor_sync(FULL_MASK, word, 2);
-        word |= __shfl_xor_sync(FULL_MASK, word, 4);
-        if ((lane & 7) == 0) kcodes[(size_t)(r0 + r) * (D / 8) + c / 8] = word;
+      for (int c = 0; c < 8; ++c) {
+        lo[c] = fminf(lo[c], x[k][c]);
+        hi[c] = fmaxf(hi[c], x[k][c]);
       }
+  }
+  GroupQuant q[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+#pragma unroll
+    for (int o = OCT; o < 32; o <<= 1) {                     // across the row groups
+      lo[c] = fminf(lo[c], __shfl_xor_sync(FULL_MASK, lo[c], o));
+      hi[c] = fmaxf(hi[c], __shfl_xor_sync(FULL_MASK, hi[c], o));
+    }
+    q[c] = group_params(lo[c], hi[c]);
+  }
+  if (rg == 0) {
+    uint32_t sv[4], mv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 s2 = __halves2half2(q[2 * e].s16, q[2 * e + 1].s16);
+      const __half2 m2 = __halves2half2(q[2 * e].m16, q[2 * e + 1].m16);
+      sv[e] = *reinterpret_cast<const uint32_t*>(&s2);
+      mv[e] = *reinterpret_cast<const uint32_t*>(&m2);
+    }
+    *reinterpret_cast<uint4*>(kmeta + 8 * oct) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
+    *reinterpret_cast<uint4*>(kmeta + D + 8 * oct) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
+  }
+#pragma unroll 1
+  for (int r0 = 0; r0 < BS; r0 += KR) {
+    if (BS > KR) load_chunk(r0);                             // else the rows are still in registers
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) word |= quant_code(x[k][c], q[c]) << (4 * nibble_of(c));
+      kcodes[(size_t)(r0 + rg + RG * k) * (D / 8) + oct] = word;
     }
   }
 }
