@@ -4,9 +4,10 @@
 // decode_common.cuh).  A producer walks the piece with a cursor, reads block-table
 // entries 32 at a time (and the next 32 ahead), and for each position issues two TMA
 // tensor loads per 64-channel box (K and V, 128-byte swizzle) into a ring of `stages`
-// shared-memory slots guarded by full/empty mbarriers.  The producer is a warp of its
-// own for groups of up to 8 heads and consumer warp 0 otherwise.  Consumer warps split
-// the group's heads (8 or 16 each), so one K/V read serves every head of the group.
+// shared-memory slots guarded by full/empty mbarriers (for groups of 17-32 heads at block
+// size 16, a slot holds two consecutive blocks of a segment).  The producer is a warp of
+// its own for groups of up to 32 heads and consumer warp 0 above that.  Consumer warps
+// split the group's heads (8 or 16 each), so one K/V read serves every head of the group.
 //
 // Per block, token-major: S^T = K Q^T with mma.m16n8k16 (the block's tokens on M, heads
 // on N; bf16 in, fp32 accumulate; K A-fragments by ldmatrix from the swizzled tile),

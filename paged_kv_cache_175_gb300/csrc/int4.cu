@@ -244,9 +244,10 @@ __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a
 //
 // Same partition, producer and token-major tiles as the bf16 kernel.  A stage holds one
 // (block, kv head) record -- K codes [BS][D/2], V codes [BS][D/2], K meta [2][D] fp16,
-// V meta [BS][2] fp16 -- moved by one 1-D bulk copy.  A sequence's unfinished last block
-// has no K codes: its K rows are read from the bf16 tail straight from L2 (the producer
-// prefetches them when it enters the segment), so the ring holds no tail space.
+// V meta [BS][2] fp16 -- moved by one 1-D bulk copy, or with TB = 2 two records of
+// consecutive blocks of one segment.  A sequence's unfinished last block has no K codes:
+// its K rows are read from the bf16 tail straight from L2 (the producer prefetches them
+// when it enters the segment), so the ring holds no tail space.
 //
 // S^T = K^ Q^T uses fp16 mma.  The channel order inside a k-step is chosen so each
 // thread's A-fragment rows come from one 16-byte load of a token row: thread t of a quad
