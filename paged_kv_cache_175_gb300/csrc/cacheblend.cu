@@ -10,8 +10,16 @@
 
 namespace pkv {
 
-// ---- deviation: one warp per token, 16-byte vectors, every load of a pass in flight --------
+// ---- deviation: a group of lanes per token, 16-byte vectors, every load of a pass in flight --
+// A token's K and V rows (n_kv * head_dim / 8 vectors each) go to `lpt` lanes, the
+// smallest power of two covering them, at most 32; a warp takes 32 / lpt tokens at once.
 constexpr int kDevThreads = 256;
+
+__host__ __device__ inline int dev_lanes_per_token(int vec_per_tok) {
+  int l = 4;
+  while (l < 32 && l < vec_per_tok) l <<= 1;
+  return l;
+}
 
 __global__ void __launch_bounds__(kDevThreads)
     kv_deviation_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
@@ -19,28 +27,27 @@ __global__ void __launch_bounds__(kDevThreads)
                         const uint4* __restrict__ v_new, long long n, int n_kv, int block_size, int vec_per_row,
                         long long n_slots, float* __restrict__ dev, int32_t* err) {
   const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (kDevThreads / 32);
   const int vec_per_tok = n_kv * vec_per_row;
-  for (long long t = blockIdx.x * (long long)(kDevThreads / 32) + (threadIdx.x >> 5); t < n; t += warps) {
-    const long long slot = slots[t];
-    if (slot < 0 || slot >= n_slots) {
-      if (lane == 0) {
-        set_err(err, PKV_DEV_BAD_SLOT);
-        dev[t] = 0.f;
-      }
-      continue;
-    }
-    const long long blk = slot / block_size, row = slot - blk * block_size;
-    const uint4* kn = k_new + t * vec_per_tok;
-    const uint4* vn = v_new + t * vec_per_tok;
+  const int lpt = dev_lanes_per_token(vec_per_tok), tpw = 32 / lpt;
+  const int sub = lane / lpt, sl = lane % lpt;
+  const long long step = (long long)gridDim.x * (kDevThreads / 32) * tpw;
+  for (long long t0 = (blockIdx.x * (long long)(kDevThreads / 32) + (threadIdx.x >> 5)) * tpw; t0 < n;
+       t0 += step) {
+    const long long t = t0 + sub;
+    const long long slot = t < n ? slots[t] : 0;
+    const bool bad = t < n && (slot < 0 || slot >= n_slots);
+    const bool live = t < n && !bad;
+    const long long blk = live ? slot / block_size : 0, row = live ? slot - blk * block_size : 0;
+    const uint4* kn = k_new + (live ? t : 0) * vec_per_tok;
+    const uint4* vn = v_new + (live ? t : 0) * vec_per_tok;
     float acc = 0.f;
-    for (int base = 0; base < vec_per_tok; base += 64) {
+    for (int base = 0; base < vec_per_tok; base += 2 * lpt) {
       uint4 a[2], b[2], c[2], d[2];
       bool ok[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int i = base + u * 32 + lane;
-        ok[u] = i < vec_per_tok;
+        const int i = base + u * lpt + sl;
+        ok[u] = live && i < vec_per_tok;
         if (ok[u]) {
           const int g = i / vec_per_row, w = i - g * vec_per_row;
           const size_t src = (((size_t)blk * n_kv + g) * block_size + row) * vec_per_row + w;
@@ -68,9 +75,11 @@ __global__ void __launch_bounds__(kDevThreads)
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);
-    if (lane == 0) dev[t] = sqrtf(acc);
+    for (int o = lpt / 2; o; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);   // within the group
+    if (sl == 0 && t < n) {
+      if (bad) set_err(err, PKV_DEV_BAD_SLOT);
+      dev[t] = bad ? 0.f : sqrtf(acc);
+    }
   }
 }
 
@@ -252,8 +261,8 @@ extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, c
   if (!k_pool || !v_pool || !slots || !k_new || !v_new || !dev) return PKV_EINVAL;
   if (!al16(k_pool) || !al16(v_pool) || !al16(k_new) || !al16(v_new)) return PKV_EINVAL;
   const int vpr = head_dim / 8;
-  const int warps_per_cta = kDevThreads / 32;
-  const long long want = ((long long)n + warps_per_cta - 1) / warps_per_cta;
+  const int tokens_per_cta = kDevThreads / 32 * (32 / dev_lanes_per_token(n_kv * vpr));
+  const long long want = ((long long)n + tokens_per_cta - 1) / tokens_per_cta;
   const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
   kv_deviation_kernel<<<grid, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), slots, static_cast<const uint4*>(k_new),
