@@ -675,11 +675,12 @@ def main():
     assert int(main_step.err.item()) == 0, f"device error flag {int(main_step.err.item())}"
 
     # ---- end to end through the public API: pinned host inputs in, output back out ----
-    # Every step copies its inputs in from pinned host memory and its result back out.  Steps
-    # run in pairs, each pair one CUDA graph: step 1's inputs go in on a side stream while
-    # step 0's kernels run, and step 0's result goes out while step 1's kernels run (the
-    # pipelining of a serving loop); the inputs travel packed in one pinned buffer per step
-    # (one copy; the device-side tensors are views of one device buffer).
+    # Every step copies its inputs in from pinned host memory and its result back out,
+    # double-buffered on a second stream: step j+1's inputs go in while step j's kernels run,
+    # and step j's result comes out while step j+1's kernels run (the pipelining of a serving
+    # loop).  The inputs travel packed in one pinned buffer per step (one copy; the
+    # device-side tensors are views of one device buffer); the launches of G steps are one
+    # CUDA graph.
     w = main_step.w
     layout, off = {}, 0
     for k, v in main_step.inputs.items():
@@ -707,50 +708,63 @@ def main():
 
     def one_step(b):                                      # a step on its own, copies in order
         d_pack[b].copy_(h_pack, non_blocking=True)
+        flush()
         main_step.step(step_args(b))
         if has_out:
             out_h[b].copy_(out_d[b], non_blocking=True)
 
-    ev_k0, ev_in1 = torch.cuda.Event(), torch.cuda.Event()
+    # G steps per graph launch: the double-buffered pipeline below runs inside each graph,
+    # so G only sets how often the first input copy and the last result copy are exposed
+    G = 8
+    ev_k = [torch.cuda.Event() for _ in range(G)]
+    ev_in = [torch.cuda.Event() for _ in range(G)]
+    ev_out = [torch.cuda.Event() for _ in range(G)]
 
-    def two_steps():                                      # a pair, copies beside the other step's kernels
+    def group_steps():                                    # steps j = 0..G-1 on buffers j % 2
         cs = torch.cuda.current_stream()
         copy_stream.wait_stream(cs)
         d_pack[0].copy_(h_pack, non_blocking=True)
-        with torch.cuda.stream(copy_stream):
-            d_pack[1].copy_(h_pack, non_blocking=True)
-            ev_in1.record(copy_stream)
-        main_step.step(step_args(0))
-        ev_k0.record(cs)
-        cs.wait_event(ev_in1)
-        main_step.step(step_args(1))
-        if has_out:
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(ev_k0)
-                out_h[0].copy_(out_d[0], non_blocking=True)
-            out_h[1].copy_(out_d[1], non_blocking=True)
+        for j in range(G):
+            if j + 1 < G:                                 # step j+1's inputs, once step j-1 is done with the buffer
+                with torch.cuda.stream(copy_stream):
+                    if j >= 1:
+                        copy_stream.wait_event(ev_k[j - 1])
+                    d_pack[(j + 1) % 2].copy_(h_pack, non_blocking=True)
+                    ev_in[j + 1].record(copy_stream)
+            if j >= 1:
+                cs.wait_event(ev_in[j])
+            if j >= 2 and has_out:
+                cs.wait_event(ev_out[j - 2])              # step j-2's result has left out_d[j % 2]
+            flush()                                       # as between the device-timed steps
+            main_step.step(step_args(j % 2))
+            ev_k[j].record(cs)
+            if has_out:                                   # step j's result, beside step j+1's kernels
+                with torch.cuda.stream(copy_stream):
+                    copy_stream.wait_event(ev_k[j])
+                    out_h[j % 2].copy_(out_d[j % 2], non_blocking=True)
+                    ev_out[j].record(copy_stream)
         cs.wait_stream(copy_stream)
 
     def e2e_run(n):
-        for _ in range(n // 2):
+        for _ in range(n // G):
             if graph is not None:
                 graph.replay()
             else:
-                two_steps()
-        if n % 2:
+                group_steps()
+        for _ in range(n % G):
             one_step(0)
 
     graph = None
-    e2e_run(max(W, 4))                                    # eager warm-up (sets up the library's kernels)
+    e2e_run(max(W, G))                                    # eager warm-up (sets up the library's kernels)
     torch.cuda.synchronize()
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            two_steps()
+            group_steps()
         graph = g
-        e2e_run(2)
+        e2e_run(G)
         torch.cuda.synchronize()
-        e2e_mode = "one CUDA graph per pair of steps, replayed"
+        e2e_mode = f"one CUDA graph per group of {G} steps, replayed"
     except Exception as ex:                               # eager launches if capture is refused
         graph = None
         torch.cuda.synchronize()
@@ -783,8 +797,8 @@ def main():
         "frac_of_hbm_peak": round(agg["gbs"] / world / peak, 4),
         "e2e": {"value": round(e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "launch": e2e_mode,
-                "copies": "inputs packed in one pinned buffer per step; in each pair of steps, step 1's inputs "
-                          "go in and step 0's result comes out on a second stream beside the other step's kernels",
+                "copies": "inputs packed in one pinned buffer per step; double-buffered on a second stream: "
+                          "step j+1's inputs go in and step j's result comes out beside the kernels",
                 "ms_per_step": round(e2e["ms_per_step"], 5)},
         "roofline": {"bound": "hbm", "kernel": {"Bf16Step": "paged_decode_attn (attention + split-reduce)",
                                                 "Int4Step": "paged_decode_attn_int4 (attention + split-reduce)",
