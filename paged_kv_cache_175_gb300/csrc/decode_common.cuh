@@ -17,13 +17,13 @@
 namespace pkv {
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_VALID = 8 };
-// INT4 stages of two blocks: F_PAIR marks a stage holding the next block of the same
-// segment too; F_END marks the last stage of a piece.
+// Ring stages of up to two blocks: F_PAIR marks a stage that also holds the next block of
+// the same segment; F_END marks the last stage of a piece.
 enum : int { F_PAIR = 16, F_END = 32 };
 // Lazy softmax offset (base-2 units): the attention kernels raise a head's running offset
-// only when a score exceeds it by more than this, so exponentials stay below 2^8 (inside
-// the range of the fp16 high + low split of P) and most tiles skip the max reduction and
-// the rescale.  Softmax itself does not depend on the offset.
+// only when a score exceeds it by more than this, so exponentials stay below 2^8 (well
+// inside the range of the fp16 / bf16 high + low split of P) and most tiles skip the max
+// reduction and the rescale.  Softmax itself does not depend on the offset.
 constexpr float kLazyMax = 8.f;
 
 struct DecodeArgs {

@@ -302,7 +302,9 @@ __host__ __device__ constexpr size_t int4_smem_bytes(int stages) {
 
 // TB = 2: a stage holds two consecutive blocks of one segment when the piece has them
 // (32 token rows per pass at block size 16: the per-stage loop, barrier, producer and
-// softmax work is shared by twice the tokens).
+// softmax work is shared by twice the tokens).  Single-warp CTAs are bounded to 12 per SM
+// with two-block stages (170 registers) and 16 per SM with one-block stages at block size
+// 16 (128 registers).
 template <int D, int BS, int NH, int MT, int TB>
 __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 && NH == 1 ? 16 : 0))
     decode_int4_kernel(const DecodeArgs a) {
