@@ -71,7 +71,8 @@ int pkv_last_cuda_error(void);
 
 /*
  * kv_append — write each new token's K and V rows into the pools at its slot.
- * Decode-step listing, "append" line (see file header).
+ * "KV Cache는 왜 LLM 서빙의 핵심인가", section "KV Cache: O(T²)를 O(T)로": the append
+ * of the new token's k_t, v_t in each decode step (see file header).
  *   k, v          bf16 [n_tok][n_kv][head_dim]
  *   slot_mapping  int64 [n_tok]; slot = physical block * block_size + row.
  *                 A negative slot is padding and is skipped.  Slots must be distinct.
@@ -90,7 +91,9 @@ size_t pkv_decode_workspace_bytes(int batch, int n_h, int n_kv, int head_dim, in
 
 /*
  * paged_decode_attn — one decode step of attention over a paged bf16 cache.
- * Decode-step listing, attention line; PagedAttention blocks; GQA groups.
+ * "KV Cache는 왜 LLM 서빙의 핵심인가", section "KV Cache: O(T²)를 O(T)로": the attention
+ * of each decode step over the whole cache; PagedAttention blocks; GQA groups (see file
+ * header).
  *   q             bf16 [batch][n_h][head_dim]
  *   k_pool,v_pool bf16 [num_blocks][n_kv][block_size][head_dim]
  *   block_tables  int32 [batch][max_blocks]; entry i of row s is the physical block
