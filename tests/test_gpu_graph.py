@@ -1,5 +1,6 @@
 """A decode step (append + attention) captured in a CUDA graph and replayed gives the same
-bits as the same calls launched eagerly (bf16 and INT4 caches)."""
+bits as the same calls launched eagerly (bf16 and INT4 caches), and repeated calls give the
+same bits."""
 import numpy as np
 import pytest
 import torch
@@ -81,3 +82,43 @@ def test_int4_step_graph_equals_eager():
     for a, b in zip((caches[0].k_codes, caches[0].v_codes, caches[0].k_meta, caches[0].v_meta, caches[0].k_tail),
                     (caches[1].k_codes, caches[1].v_codes, caches[1].k_meta, caches[1].v_meta, caches[1].k_tail)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["mqa_bs16", "llama3_8b_b16"])
+def test_repeated_calls_are_bitwise_identical(name):
+    """The partition, the ring and the merge order are fixed, so repeated calls give the same
+    bits (a race on a reused ring slot would show up here as a difference)."""
+    w = workloads.make(name, 0)
+    kp, vp = workloads.pools_bf16(w, 0, DEV)
+    q = workloads.queries(w, 0, DEV)
+    bt = torch.as_tensor(w.block_tables, device=DEV)
+    ctx = torch.as_tensor(w.context_lens, device=DEV)
+    err = err_flag()
+    ref = pkv.paged_decode_attn(q, kp, vp, bt, ctx, w.scale, out_dtype=torch.float32, err=err)
+    outs = [pkv.paged_decode_attn(q, kp, vp, bt, ctx, w.scale, out_dtype=torch.float32, err=err) for _ in range(20)]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert all(torch.equal(o, ref) for o in outs)
+
+
+def test_repeated_int4_calls_are_bitwise_identical():
+    w = workloads.make("int4_long_b8", 0)
+    bs = w.block_size
+    cache = pkv.alloc_int4_cache(w.num_blocks, w.n_kv, bs, w.head_dim, w.batch, DEV)
+    ks, vs, sl, tl = [], [], [], []
+    for s in range(w.batch):
+        k, v = workloads.history_kv(w, s, 0, DEV)
+        slots = workloads.history_slots(w, s)
+        ks.append(k); vs.append(v); sl.append(slots); tl.append(np.full(len(slots), s, np.int32))
+    pkv.kv_quant_append_int4(torch.cat(ks), torch.cat(vs), torch.as_tensor(np.concatenate(sl), device=DEV),
+                             torch.as_tensor(np.concatenate(tl), device=DEV), cache)
+    q = workloads.queries(w, 0, DEV)
+    bt = torch.as_tensor(w.block_tables, device=DEV)
+    ctx = torch.as_tensor(w.context_lens, device=DEV)
+    err = err_flag()
+    ref = pkv.paged_decode_attn_int4(q, cache, bt, ctx, w.scale, out_dtype=torch.float32, err=err)
+    outs = [pkv.paged_decode_attn_int4(q, cache, bt, ctx, w.scale, out_dtype=torch.float32, err=err)
+            for _ in range(20)]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert all(torch.equal(o, ref) for o in outs)
