@@ -25,7 +25,9 @@ __global__ void __launch_bounds__(kDevThreads)
     kv_deviation_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
                         const int64_t* __restrict__ slots, const uint4* __restrict__ k_new,
                         const uint4* __restrict__ v_new, long long n, int n_kv, int block_size, int vec_per_row,
-                        long long n_slots, float* __restrict__ dev, int32_t* err) {
+                        long long n_slots, int bs_shift, int vpr_shift, float* __restrict__ dev, int32_t* err) {
+  // bs_shift / vpr_shift: log2 of block_size / vec_per_row when they are powers of two
+  // (every shape the attention kernels take), else -1 and the index math divides
   const int lane = threadIdx.x & 31;
   const int vec_per_tok = n_kv * vec_per_row;
   const int lpt = dev_lanes_per_token(vec_per_tok), tpw = 32 / lpt;
@@ -37,7 +39,11 @@ __global__ void __launch_bounds__(kDevThreads)
     const long long slot = t < n ? slots[t] : 0;
     const bool bad = t < n && (slot < 0 || slot >= n_slots);
     const bool live = t < n && !bad;
-    const long long blk = live ? slot / block_size : 0, row = live ? slot - blk * block_size : 0;
+    long long blk = 0, row = 0;
+    if (live) {
+      blk = bs_shift >= 0 ? slot >> bs_shift : slot / block_size;
+      row = slot - blk * block_size;
+    }
     const uint4* kn = k_new + (live ? t : 0) * vec_per_tok;
     const uint4* vn = v_new + (live ? t : 0) * vec_per_tok;
     float acc = 0.f;
@@ -49,7 +55,7 @@ __global__ void __launch_bounds__(kDevThreads)
         const int i = base + u * lpt + sl;
         ok[u] = live && i < vec_per_tok;
         if (ok[u]) {
-          const int g = i / vec_per_row, w = i - g * vec_per_row;
+          const int g = vpr_shift >= 0 ? i >> vpr_shift : i / vec_per_row, w = i - g * vec_per_row;
           const size_t src = (((size_t)blk * n_kv + g) * block_size + row) * vec_per_row + w;
           a[u] = __ldg(k_pool + src);
           b[u] = __ldg(v_pool + src);
@@ -252,6 +258,12 @@ __global__ void __launch_bounds__(256) kv_fuse_kernel(const uint4* __restrict__ 
 using namespace pkv;
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static int log2_if_pow2(int x) {
+  if (x <= 0 || (x & (x - 1))) return -1;
+  int k = 0;
+  while ((1 << k) < x) ++k;
+  return k;
+}
 
 extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, const int64_t* slots,
                                        const void* k_new, const void* v_new, int n, int num_blocks, int block_size,
@@ -266,8 +278,8 @@ extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, c
   const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
   kv_deviation_kernel<<<grid, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), slots, static_cast<const uint4*>(k_new),
-      static_cast<const uint4*>(v_new), n, n_kv, block_size, vpr, (long long)num_blocks * block_size, dev,
-      err_flag);
+      static_cast<const uint4*>(v_new), n, n_kv, block_size, vpr, (long long)num_blocks * block_size,
+      log2_if_pow2(block_size), log2_if_pow2(vpr), dev, err_flag);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
