@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kDevThreads)
                         long long n_slots, int bs_shift, int vpr_shift, float* __restrict__ dev, int32_t* err) {
   // bs_shift / vpr_shift: log2 of block_size / vec_per_row when they are powers of two
   // (every shape the attention kernels take), else -1 and the index math divides
+  grid_dep_launch();                       // a following selection may launch; it waits for this grid
   const int lane = threadIdx.x & 31;
   const int vec_per_tok = n_kv * vec_per_row;
   const int lpt = dev_lanes_per_token(vec_per_tok), tpw = 32 / lpt;
@@ -140,6 +141,8 @@ __global__ void __launch_bounds__(kSelThreads)
   __shared__ int total;
   __shared__ unsigned long long prefix_sh;
   __shared__ int remain_sh, done_sh;
+  grid_dep_wait();                         // the deviations come from the kernel before this one
+  grid_dep_launch();
   const int s = blockIdx.x;
   const int lo = seg_offsets[s], hi = seg_offsets[s + 1];
   const int n = hi > lo ? hi - lo : 0;
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(256) kv_fuse_kernel(const uint4* __restrict__ 
                                                       int vec_per_row, int n_kv, int block_size, long long n_slots,
                                                       long long n_rows, uint4* __restrict__ k_pool,
                                                       uint4* __restrict__ v_pool, int32_t* err) {
+  grid_dep_wait();                         // the selected rows come from the kernel before this one
   const int vec_per_tok = vec_per_row * n_kv;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -293,9 +297,9 @@ extern "C" pkv_status pkv_select_top(const float* dev, const int32_t* seg_offset
   if (n_seg < 0) return PKV_EINVAL;
   if (n_seg == 0) return PKV_OK;
   if (!dev || !seg_offsets || !counts || !out) return PKV_EINVAL;
-  select_top_kernel<<<n_seg, kSelThreads, 0, static_cast<cudaStream_t>(stream)>>>(dev, seg_offsets, counts, n_seg,
-                                                                                  out);
-  const cudaError_t e = cudaGetLastError();
+  void* args[] = {(void*)&dev, (void*)&seg_offsets, (void*)&counts, (void*)&n_seg, (void*)&out};
+  const cudaError_t e = launch_pdl((const void*)select_top_kernel, dim3(n_seg), dim3(kSelThreads), 0,
+                                   static_cast<cudaStream_t>(stream), args);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return PKV_ECUDA;
@@ -315,11 +319,16 @@ extern "C" pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, const in
   const long long total = (long long)n_sel * n_kv * vpr;
   const long long want = (total + 255) / 256;
   const int grid = (int)(want < 32LL * device_sm_count() ? want : 32LL * device_sm_count());
-  kv_fuse_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), row_slots, rows, total, vpr, n_kv,
-      block_size, (long long)num_blocks * block_size, n_rows, static_cast<uint4*>(k_pool),
-      static_cast<uint4*>(v_pool), err_flag);
-  const cudaError_t e = cudaGetLastError();
+  const uint4* kn = static_cast<const uint4*>(k_new);
+  const uint4* vn = static_cast<const uint4*>(v_new);
+  uint4* kp = static_cast<uint4*>(k_pool);
+  uint4* vp = static_cast<uint4*>(v_pool);
+  long long n_slots = (long long)num_blocks * block_size, rows_ll = n_rows;
+  void* args[] = {(void*)&kn, (void*)&vn, (void*)&row_slots, (void*)&rows, (void*)&total, (void*)&vpr,
+                  (void*)&n_kv, (void*)&block_size, (void*)&n_slots, (void*)&rows_ll, (void*)&kp, (void*)&vp,
+                  (void*)&err_flag};
+  const cudaError_t e = launch_pdl((const void*)kv_fuse_kernel, dim3(grid), dim3(256), 0,
+                                   static_cast<cudaStream_t>(stream), args);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return PKV_ECUDA;
