@@ -66,6 +66,7 @@ struct QuantAppendArgs {
 // appended earlier in this call from `k` and older rows from the tail.
 template <int D, int BS>
 __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs a) {
+  grid_dep_launch();                            // the tail update may launch; it waits for this grid
   constexpr int CPL = D / 32;                   // V channels per lane
   constexpr int LPW = 8 / CPL;                  // lanes per 32-bit code word
   const int lane = threadIdx.x & 31;
@@ -218,7 +219,10 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
 // Phase 2: K rows of blocks that stay unfinished after this call go to the tail.
 template <int D>
 __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a) {
-  grid_dep_launch();                       // the attention's setup may overlap this kernel
+  // The tail rows of a block this call completes are read by phase 1: wait for it before
+  // writing any.  The attention's setup may overlap this kernel.
+  grid_dep_wait();
+  grid_dep_launch();
   constexpr int VEC = D / 8;                                 // 16-byte vectors per row
   const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= (long long)a.n_tok * a.n_kv * VEC) return;
@@ -835,8 +839,13 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
   if (head_dim == d && block_size == b) quant_append_kernel<d, b><<<g1, 256, 0, st>>>(a);
   PKV_Q(128, 16) PKV_Q(128, 32) PKV_Q(128, 64) PKV_Q(64, 16) PKV_Q(64, 32) PKV_Q(64, 64)
 #undef PKV_Q
-  if (head_dim == 128) tail_write_kernel<128><<<g2, 256, 0, st>>>(a);
-  else tail_write_kernel<64><<<g2, 256, 0, st>>>(a);
+  void* targs[] = {(void*)&a};
+  cudaError_t e2 = launch_pdl(head_dim == 128 ? (const void*)tail_write_kernel<128> : (const void*)tail_write_kernel<64>,
+                              dim3(g2), dim3(256), 0, st, targs);
+  if (e2 != cudaSuccess) {
+    record_cuda_error(e2);
+    return PKV_ECUDA;
+  }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
