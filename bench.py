@@ -173,6 +173,24 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bench_probes(dev, stream, nbytes=4 << 30, K=10, W=3):
+    """The library's HBM ceiling probes on a buffer of nbytes (31x the L2 at the default):
+    a read-only stream and a copy of half the buffer into the other half; best of K."""
+    import paged_kv_cache_175_gb300 as pkv
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    half = nbytes // 2
+    src, dst = buf[:half], buf[half:]
+    none = lambda: None
+    t_read = min(time_steps(lambda: pkv.probe_read(buf), K, W, none, stream))
+    t_copy = min(time_steps(lambda: pkv.probe_copy(src, dst), K, W, none, stream))
+    del buf, src, dst
+    torch.cuda.empty_cache()
+    return {"read_gbs": round(nbytes / (t_read / 1e3) / 1e9, 1),
+            "copy_gbs": round(2 * half / (t_copy / 1e3) / 1e9, 1),
+            "bytes": nbytes, "best_of": K, "launches": 2 * (K + W)}
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_kv_cache_175_gb300", "csrc")
@@ -432,6 +450,22 @@ def cpu_samples(name, seed, n_seqs):
     return out
 
 
+def blas_threads():
+    """Threads numpy's BLAS runs with (threadpoolctl where installed, else the usual
+    environment variables, else the host's core count, which OpenBLAS defaults to)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [int(i["num_threads"]) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
 def time_cpu(samples, budget_s):
     """Run the oracle's decode step over the samples (cycling) until budget_s seconds."""
     import oracle
@@ -447,9 +481,10 @@ def time_cpu(samples, budget_s):
         elapsed += time.perf_counter() - t0
         nbytes += attention_bytes(sub) + append_bytes(sub)
         done += 1
-    cores = max(1, int(round((ru() - cpu0) / max(time.perf_counter() - wall0, 1e-9))))
+    util = (ru() - cpu0) / max(time.perf_counter() - wall0, 1e-9)
     info = {"sample": f"{done} sequence decode steps (append + attention, all heads) of the {samples[0][0].name} "
-                      f"workload, {elapsed:.1f} s of oracle time", "cores": cores, "kind": "oracle"}
+                      f"workload, {elapsed:.1f} s of oracle time", "cores": os.cpu_count(),
+            "blas_threads": blas_threads(), "cpu_time_per_wall_time": round(util, 2), "kind": "oracle"}
     return nbytes / elapsed / 1e9, done / elapsed, elapsed, info
 
 
@@ -609,6 +644,42 @@ def run_config(name, K, W, seed, dev, stream, flush_buf, world):
     return st, step_bytes, attn_bytes, agg, attn_ms
 
 
+STEP_NAMES = {"Bf16Step": "kv_append + paged_decode_attn",
+              "Int4Step": "kv_quant_append_int4 + paged_decode_attn_int4",
+              "RopeStep": "rope_shift_k",
+              "BlendStep": "kv_deviation + select_top + kv_fuse"}
+
+
+def step_class_name(name):
+    if name.startswith("int4"):
+        return "Int4Step"
+    if name.startswith("rope_"):
+        return "RopeStep"
+    if name.startswith("blend_"):
+        return "BlendStep"
+    return "Bf16Step"
+
+
+def workload_config(name, world):
+    """The `config` object of the JSON line (both arms print the same one)."""
+    import workloads as wl
+    cls = step_class_name(name)
+    w = wl.make(name[5:] if cls == "RopeStep" else name[6:] if cls == "BlendStep" else name, 0)
+    if cls == "Bf16Step":
+        step_bytes = attention_bytes(w) + append_bytes(w)
+    elif cls == "Int4Step":
+        step_bytes = attention_bytes(w, True) + append_bytes(w, True)
+    else:
+        step_bytes = None
+    l2 = ("no flush: each step streams >= 4x the L2 (inputs larger than L2)"
+          if step_bytes is not None and step_bytes >= 4 * L2_BYTES else
+          "L2 flushed between steps (write of 2x L2, then read back; outside the events)")
+    return {"workload": f"{name}: {w.n_h} q / {w.n_kv} kv heads, head_dim {w.head_dim}, block "
+                        f"{w.block_size}, batch {w.batch}, ctx mean {float(np.mean(w.context_lens)):.0f}",
+            "step": STEP_NAMES[cls], "parallelism": f"replicas x{world}", "l2": l2,
+            "algorithmic_bytes_per_step": step_bytes}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,6 +689,10 @@ def main():
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--configs", default="all", choices=["all", "main"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--probe-only", action="store_true", help="only the HBM ceiling probes (one JSON line)")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="only W + K steps of --workload, no end-to-end, probe or other workloads (for profilers)")
+    ap.add_argument("--probe-bytes", type=int, default=4 << 30, help="buffer of the ceiling probes")
     args = ap.parse_args()
     K, W = args.steps, max(args.warmup, 0)
     world, rank, local = dist_setup(args.gpus)
@@ -640,10 +715,11 @@ def main():
             "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1, "steps": K,
             "warmup": W, "ms_per_step": round(tot / K * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_per_step": info["sample"]},
+            "config": workload_config(args.workload, 1),
             "seqs_per_s": round(statistics.mean(sps), 3),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": info["cores"], "kind": "oracle",
-                             "sample": info["sample"]},
+                             "sample": f"each step: {info['sample']}", "blas_threads": info["blas_threads"],
+                             "cpu_time_per_wall_time": info["cpu_time_per_wall_time"]},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
 
@@ -658,11 +734,24 @@ def main():
     stream = torch.cuda.current_stream()
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     peak, peak_src = measured_hbm_peak()
+    if args.probe_only:
+        pr = bench_probes(dev, stream, args.probe_bytes, K, W)
+        if rank == 0:
+            print(json.dumps({"probes": pr, "measured_copy_gbs": peak}))
+        return
 
     # ---- main workload: timed steps with clocks sampled during the timed region ----
     main_step = make_step(args.workload, rank, dev)
     step_bytes, attn_bytes = main_step.bytes()
     flush, l2_note = l2_policy(step_bytes, flush_buf)
+    if args.kernel_only:
+        ms = time_steps(main_step.step, K, W, flush, stream)
+        assert int(main_step.err.item()) == 0, f"device error flag {int(main_step.err.item())}"
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "steps": K, "warmup": W,
+                              "ms_per_step": round(statistics.mean(ms), 5),
+                              "step_gbs": round(step_bytes / (statistics.mean(ms) / 1e3) / 1e9, 2)}))
+        return
     torch.cuda.synchronize()
     barrier(world)
     with ClockSampler(local) as clk:
@@ -780,19 +869,15 @@ def main():
     e2e_total = reduce_max(e0.elapsed_time(e1), world)
     e2e = aggregate(step_bytes, w.batch, e2e_total, world, K)
 
+    probes = bench_probes(dev, stream)
+    ceiling = max(probes["read_gbs"], peak)
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9
+
     line = {
         "metric": METRIC, "value": round(agg["gbs"], 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(agg["ms_per_step"], 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {w.n_h} q / {w.n_kv} kv heads, head_dim {w.head_dim}, block "
-                               f"{w.block_size}, batch {w.batch}, ctx mean {float(np.mean(w.context_lens)):.0f}",
-                   "step": {"Bf16Step": "kv_append + paged_decode_attn",
-                            "Int4Step": "kv_quant_append_int4 + paged_decode_attn_int4",
-                            "RopeStep": "rope_shift_k",
-                            "BlendStep": "kv_deviation + select_top + kv_fuse"}[type(main_step).__name__],
-                   "parallelism": f"replicas x{world}",
-                   "l2": l2_note,
-                   "algorithmic_bytes_per_step": step_bytes},
+        "config": workload_config(args.workload, world),
         "seqs_per_s": round(agg["seqs_per_s"], 1),
         "frac_of_hbm_peak": round(agg["gbs"] / world / peak, 4),
         "e2e": {"value": round(e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -809,9 +894,16 @@ def main():
                      else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(attn_bytes / (attn_ms / 1e3) / 1e9 / peak, 4),
                      "traffic": recorded_traffic(args.workload),
-                     "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 5)},
-        # the timed loops: steps, attention alone, end to end
-        "gpu_launches": main_step.launches_per_step * 2 * K + main_step.attention_launches * K,
+                     "algorithmic_bytes_per_launch": attn_bytes, "ms_per_launch": round(attn_ms, 5),
+                     # the library's own ceiling probes, measured in this run: the attention
+                     # kernels almost only read, so the read stream is their ceiling
+                     "read_ceiling": {"kernel": "pkv_probe_read", "gbs": probes["read_gbs"],
+                                      "copy_probe_gbs": probes["copy_gbs"],
+                                      "denominator": round(ceiling, 1),
+                                      "denominator_is": "max(read probe, measured copy)",
+                                      "frac": round(achieved / ceiling, 4)}},
+        # the timed loops: steps, attention alone, end to end; the probes
+        "gpu_launches": main_step.launches_per_step * 2 * K + main_step.attention_launches * K + probes["launches"],
         "clocks": clocks,
     }
 
@@ -838,12 +930,22 @@ def main():
         line["gpu_launches"] += n_launch
         by["block_manager_llama2_70b_prefix"] = bench_block_manager(rank)
         line["by_config"] = by
+        # compact per-workload fractions of the attention call (of the measured copy / of the
+        # read ceiling), printed last so that a tail of the line still shows them
+        fr = {args.workload: (round(achieved / peak, 4), round(achieved / ceiling, 4))}
+        for k, v in by.items():
+            if "attn_gbs" in v:
+                fr[k] = (v["attn_frac"], round(v["attn_gbs"] / ceiling, 4))
 
     # ---- oracle on the host cores (rank 0, one GPU only) ----
     if rank == 0 and world == 1 and args.cpu_budget > 0 and isinstance(main_step, Bf16Step):
         g, s, el, info = time_cpu(cpu_samples(args.workload, 0, 8), args.cpu_budget)
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s", "cores": info["cores"], "kind": "oracle",
-                                "sample": info["sample"], "seqs_per_s": round(s, 3)}
+                                "sample": info["sample"], "seqs_per_s": round(s, 3),
+                                "blas_threads": info["blas_threads"],
+                                "cpu_time_per_wall_time": info["cpu_time_per_wall_time"]}
+    if args.configs == "all":
+        line["attn_frac_of_copy_and_read_ceiling"] = fr
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -150,7 +150,8 @@ pkv_status pkv_paged_decode_attn_window(const void* q, const void* k_pool, const
  *   more scratch than the array holds (pkv_decode_workspace_bytes(..., 0) >
  *   PKV_STATIC_SCRATCH_BYTES).
  *   The first call with a given device current looks up the array's device address
- *   for that device; make that call before any stream capture.
+ *   for that device (and looks it up again when the current context has changed, as
+ *   after a device reset); make that call before any stream capture.
  *   All calls share the array: calls whose GPU work can overlap (other streams, other
  *   host threads) race on it and must be serialised by the caller.
  */
@@ -161,6 +162,17 @@ pkv_status pkv_paged_decode_attn_noalloc(const void* q, const void* k_pool, cons
                                          int n_h, int n_kv, int head_dim, int block_size,
                                          int num_blocks, void* out, int out_dtype,
                                          int32_t* err_flag, void* stream);
+
+/*
+ * layer_window — the attention window of one layer from a max_attention_window list.
+ * "KV 캐시 시스템 (KV Cache System)", section "어텐션 윈도우 크기": the list gives one
+ * window per layer and is repeated over the layers when it has fewer entries than the
+ * model has layers, so layer l takes windows[l % n].  A window at least as long as a
+ * context is full attention for it (pkv_paged_decode_attn_window).
+ *   windows  host int32 [n], every entry > 0
+ * Returns the window (> 0), or -1 for a NULL list, n <= 0, layer < 0 or an entry <= 0.
+ */
+int pkv_layer_window(const int32_t* windows, int n, int layer);
 
 /*
  * kv_quant_append_int4 — quantize-on-append into an INT4 paged cache.
@@ -311,6 +323,23 @@ pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, const int64_t* row_
  * context stays usable.  PKV_EINVAL for a limit out of range or a NULL flag.
  */
 pkv_status pkv_selftest_wait(int arrive, int limit_us, int32_t* err_flag, void* stream);
+
+/*
+ * probe_read / probe_copy — the HBM bandwidth ceilings the decode kernels are measured
+ * against (the pages have no counterpart: these measure the denominator of the roofline
+ * fractions).  probe_read streams `bytes` from `buf` with 16-byte loads over a persistent
+ * grid (every SM's resident blocks, several loads in flight per thread) and folds the
+ * words into a value that is stored to *sink only in a case no data in practice gives;
+ * probe_copy copies `bytes` from `src` to `dst` with 16-byte loads and stores.  Time them
+ * with events on `stream` over buffers many times the L2: read GB/s = bytes / time,
+ * copy GB/s = 2 * bytes / time.
+ *   buf, src, dst  device memory, 16-byte aligned; src and dst must not overlap
+ *   bytes          a multiple of 16, > 0
+ *   sink           device uint32 or NULL
+ * PKV_EINVAL on a bad pointer, size or overlap.
+ */
+pkv_status pkv_probe_read(const void* buf, size_t bytes, uint32_t* sink, void* stream);
+pkv_status pkv_probe_copy(const void* src, void* dst, size_t bytes, void* stream);
 
 /* The recompute ratio max(15%, load_time / full_recompute_time), at most 1: the ratio at
  * which recomputing the selected tokens takes as long as loading the layer's KV

@@ -9,9 +9,9 @@ Functions (same names as the C entry points without the ``pkv_`` prefix):
 ``kv_append``, ``paged_decode_attn``, ``paged_decode_attn_window``,
 ``paged_decode_attn_noalloc``, ``kv_quant_append_int4``, ``paged_decode_attn_int4``,
 ``paged_decode_attn_int4_window``, ``rope_shift_k``, ``copy_blocks``, ``kv_deviation``,
-``select_top``, ``kv_fuse``, ``recompute_ratio``, ``select_count``, plus
-``decode_workspace_bytes``, ``alloc_int4_cache``, the host helper ``layer_windows``
-and ``BlockManager`` (the ``pkv_bm_*`` calls of include/pkv_bm.h).
+``select_top``, ``kv_fuse``, ``recompute_ratio``, ``select_count``, ``probe_read``,
+``probe_copy``, ``layer_window`` (as ``layer_windows``), plus
+``decode_workspace_bytes``, ``alloc_int4_cache`` and ``BlockManager`` (the ``pkv_bm_*`` calls of include/pkv_bm.h).
 """
 from __future__ import annotations
 
@@ -68,6 +68,9 @@ _SIGS = {
     "pkv_recompute_ratio": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
     "pkv_select_count": (_I, [ctypes.c_double, _I]),
     "pkv_selftest_wait": (_I, [_I, _I, _P, _P]),
+    "pkv_layer_window": (_I, [_P, _I, _I]),
+    "pkv_probe_read": (_I, [_P, ctypes.c_size_t, _P, _P]),
+    "pkv_probe_copy": (_I, [_P, _P, ctypes.c_size_t, _P]),
 }
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -158,13 +161,14 @@ def paged_decode_attn_window(q, k_pool, v_pool, block_tables, context_lens, scal
 
 
 def layer_windows(max_attention_window, n_layers):
-    """Attention window of each layer from a max_attention_window list: the list is
-    repeated when it is shorter than the model (a layer whose window is at least the
-    longest context attends to all of it)."""
-    w = [int(x) for x in max_attention_window]
-    if not w or any(x <= 0 for x in w):
+    """Attention window of each of n_layers layers from a max_attention_window list
+    (pkv_layer_window: the list repeated over the layers)."""
+    import numpy as np
+    w = np.ascontiguousarray(max_attention_window, dtype=np.int32).reshape(-1)
+    out = [lib().pkv_layer_window(w.ctypes.data, len(w), i) for i in range(max(int(n_layers), 1))]
+    if any(x < 0 for x in out):
         raise ValueError("max_attention_window must be a non-empty list of positive token counts")
-    return [w[i % len(w)] for i in range(n_layers)]
+    return out[:int(n_layers)]
 
 
 def _decode_bf16(q, k_pool, v_pool, block_tables, context_lens, scale, window, out, out_dtype, workspace, err,
@@ -198,8 +202,11 @@ def paged_decode_attn_noalloc(q, k_pool, v_pool, block_tables, context_lens, sca
     (for callers that cannot allocate device memory; concurrent calls must not overlap)."""
     _cuda(q, k_pool, v_pool, block_tables, context_lens, out, err)
     assert q.dtype == k_pool.dtype == v_pool.dtype == torch.bfloat16
+    assert block_tables.dtype == context_lens.dtype == torch.int32
     B, n_h, d = q.shape
-    num_blocks, n_kv, bs, _ = k_pool.shape
+    num_blocks, n_kv, bs, d2 = k_pool.shape
+    assert d2 == d and v_pool.shape == k_pool.shape
+    assert block_tables.dim() == 2 and block_tables.shape[0] == B and context_lens.shape == (B,)
     out, od = _out(q, out, out_dtype)
     _check("paged_decode_attn_noalloc", lib().pkv_paged_decode_attn_noalloc(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
@@ -481,3 +488,20 @@ def selftest_wait(arrive, limit_us, err, stream=None):
     """Run the bounded-wait self-test; err (device int32) gets DEV_TIMEOUT if the wait ran out."""
     _cuda(err)
     _check("selftest_wait", lib().pkv_selftest_wait(1 if arrive else 0, int(limit_us), _ptr(err), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------------------------
+# HBM ceiling probes (pkv.h): the read-only stream and the copy the roofline is measured against.
+def probe_read(buf, sink=None, stream=None):
+    """Stream every byte of the CUDA tensor `buf` once (16-byte loads)."""
+    _cuda(buf, sink)
+    _check("probe_read", lib().pkv_probe_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                              _stream(stream)))
+
+
+def probe_copy(src, dst, stream=None):
+    """Copy the CUDA tensor `src` into `dst` (same byte size; 16-byte loads and stores)."""
+    _cuda(src, dst)
+    n = src.numel() * src.element_size()
+    assert dst.numel() * dst.element_size() == n
+    _check("probe_copy", lib().pkv_probe_copy(_ptr(src), _ptr(dst), n, _stream(stream)))

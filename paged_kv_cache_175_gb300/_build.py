@@ -10,8 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu", "offload.cu", "cacheblend.cu", "block_manager.cpp"]
-HEADERS = ["pkv_device.cuh", "decode_common.cuh"]
+SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu", "offload.cu", "cacheblend.cu", "probe.cu", "block_manager.cpp"]
+HEADERS = ["pkv_device.cuh", "decode_common.cuh", "nvtx_range.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 
@@ -49,7 +49,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

@@ -2,6 +2,7 @@
 #include <cmath>
 
 #include "decode_common.cuh"
+#include "nvtx_range.h"
 
 namespace pkv {
 
@@ -98,6 +99,7 @@ static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 extern "C" pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int n_tok,
                                     void* k_pool, void* v_pool, int num_blocks, int block_size, int n_kv,
                                     int head_dim, int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_kv_append");
   if (n_tok < 0 || num_blocks < 0 || block_size <= 0 || n_kv <= 0) return PKV_EINVAL;
   if (head_dim != 64 && head_dim != 128) return PKV_EINVAL;
   if (block_size != 16 && block_size != 32 && block_size != 64) return PKV_EINVAL;
@@ -124,6 +126,7 @@ extern "C" pkv_status pkv_kv_append(const void* k, const void* v, const int64_t*
 extern "C" pkv_status pkv_rope_shift_k(void* k_pool, const int32_t* block_ids, const int32_t* deltas, int n_blocks,
                                        int num_blocks, int n_kv, int block_size, int head_dim, double rope_base,
                                        int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_rope_shift_k");
   if (n_blocks < 0 || num_blocks < 0 || n_kv <= 0) return PKV_EINVAL;
   if (head_dim != 64 && head_dim != 128) return PKV_EINVAL;
   if (block_size != 16 && block_size != 32 && block_size != 64) return PKV_EINVAL;

@@ -7,6 +7,7 @@
 
 #include "../../include/pkv.h"
 #include "decode_common.cuh"
+#include "nvtx_range.h"
 
 namespace pkv {
 
@@ -272,6 +273,7 @@ static int log2_if_pow2(int x) {
 extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, const int64_t* slots,
                                        const void* k_new, const void* v_new, int n, int num_blocks, int block_size,
                                        int n_kv, int head_dim, float* dev, int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_kv_deviation");
   if (n < 0 || num_blocks < 0 || block_size < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8) return PKV_EINVAL;
   if (n == 0) return PKV_OK;
   if (!k_pool || !v_pool || !slots || !k_new || !v_new || !dev) return PKV_EINVAL;
@@ -294,6 +296,7 @@ extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, c
 
 extern "C" pkv_status pkv_select_top(const float* dev, const int32_t* seg_offsets, const int32_t* counts, int n_seg,
                                      int32_t* out, void* stream) {
+  PKV_NVTX("pkv_select_top");
   if (n_seg < 0) return PKV_EINVAL;
   if (n_seg == 0) return PKV_OK;
   if (!dev || !seg_offsets || !counts || !out) return PKV_EINVAL;
@@ -310,6 +313,7 @@ extern "C" pkv_status pkv_select_top(const float* dev, const int32_t* seg_offset
 extern "C" pkv_status pkv_kv_fuse(const void* k_new, const void* v_new, const int64_t* row_slots, int n_rows,
                                   const int32_t* rows, int n_sel, void* k_pool, void* v_pool, int num_blocks,
                                   int block_size, int n_kv, int head_dim, int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_kv_fuse");
   if (n_sel < 0 || n_rows < 0 || num_blocks < 0 || block_size < 1 || n_kv < 1 || head_dim < 8 || head_dim % 8)
     return PKV_EINVAL;
   if (n_sel == 0) return PKV_OK;

@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "decode_common.cuh"
+#include "nvtx_range.h"
 
 namespace pkv {
 
@@ -91,10 +92,14 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
   PieceInfo pi;
   piece_setup(a, blockIdx.x, gridDim.x, warp == producer_warp, cur, pi);
   const int P = pi.P, p = blockIdx.x;
-  if (p >= P) return;
   const long long pstart = pi.pstart, pend = pi.pend;
-  const int len = (int)(pend - pstart);
-  if (len <= 0) return;
+  const int len = p < P ? (int)(pend - pstart) : 0;
+  // A CTA without work still waits for the kernel before it (in inline-plan mode its
+  // wait comes below), so no launch after this grid on the stream can pass the append.
+  if (len <= 0) {
+    if (a.inline_plan) grid_dep_wait();
+    return;
+  }
   // The setup above reads only this call's inputs; the pools may still be being written by
   // the kernel before this one on the stream (an append launched ahead of the attention),
   // so every thread waits for it here, with the piece's first block-table line on its way.
@@ -561,6 +566,7 @@ extern "C" pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, c
                                             int n_kv, int head_dim, int block_size, int num_blocks, void* out,
                                             int out_dtype, void* workspace, size_t workspace_bytes,
                                             int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_paged_decode_attn");
   return decode_bf16(q, k_pool, v_pool, block_tables, max_blocks, context_lens, scale, 0, batch, n_h, n_kv, head_dim,
                      block_size, num_blocks, out, out_dtype, workspace, workspace_bytes, err_flag, stream);
 }
@@ -571,6 +577,7 @@ extern "C" pkv_status pkv_paged_decode_attn_window(const void* q, const void* k_
                                                    int n_h, int n_kv, int head_dim, int block_size, int num_blocks,
                                                    void* out, int out_dtype, void* workspace,
                                                    size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_paged_decode_attn_window");
   return decode_bf16(q, k_pool, v_pool, block_tables, max_blocks, context_lens, scale, window, batch, n_h, n_kv,
                      head_dim, block_size, num_blocks, out, out_dtype, workspace, workspace_bytes, err_flag, stream);
 }
@@ -595,24 +602,45 @@ extern "C" pkv_status pkv_paged_decode_attn_window(const void* q, const void* k_
 // partial states the same call wrote.
 static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
 
+// The address is kept per device together with the context it was looked up in; after a
+// device reset (a new primary context, where the module and its array are loaded again)
+// the next call looks it up anew instead of passing a stale address to the kernels.
 static void* static_scratch_address() {
+  using CtxGetCurrent = CUresult (*)(CUcontext*);
+  static CtxGetCurrent ctx_get = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      ctx_get = reinterpret_cast<CtxGetCurrent>(fn);
+  });
   static std::mutex mu;
   static void* addr[64] = {};
+  static CUcontext owner[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
     record_cuda_error(e);
     return nullptr;
   }
+  // the context current now (none yet before the runtime's first call on this thread, or
+  // right after a reset); the symbol lookup below makes the primary context current
+  CUcontext ctx = nullptr;
+  if (ctx_get) ctx_get(&ctx);
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || !ctx || owner[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) {
       record_cuda_error(e);
       return nullptr;
     }
+    CUcontext now = nullptr;
+    if (ctx_get) ctx_get(&now);
     addr[dev] = p;
+    owner[dev] = now;
   }
   return addr[dev];
 }
@@ -622,6 +650,7 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(const void* q, const void* k
                                                     const int32_t* context_lens, float scale, int batch, int n_h,
                                                     int n_kv, int head_dim, int block_size, int num_blocks,
                                                     void* out, int out_dtype, int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_paged_decode_attn_noalloc");
   if (batch < 0 || !valid_shape(n_h, n_kv, head_dim, block_size)) return PKV_EINVAL;
   if (batch == 0) return PKV_OK;
   const size_t need = pkv_decode_workspace_bytes(batch, n_h, n_kv, head_dim, block_size, 0);

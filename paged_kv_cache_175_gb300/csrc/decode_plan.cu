@@ -342,3 +342,12 @@ extern "C" pkv_status pkv_selftest_wait(int arrive, int limit_us, int32_t* err_f
   }
   return PKV_OK;
 }
+
+// Window of one layer from a per-layer list of attention windows that is repeated over the
+// layers when it is shorter than the model.
+extern "C" int pkv_layer_window(const int32_t* windows, int n, int layer) {
+  if (!windows || n <= 0 || layer < 0) return -1;
+  for (int i = 0; i < n; ++i)
+    if (windows[i] <= 0) return -1;
+  return windows[layer % n];
+}

@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "decode_common.cuh"
+#include "nvtx_range.h"
 
 namespace pkv {
 
@@ -348,10 +349,14 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
   PieceInfo pi;
   piece_setup(a, blockIdx.x, gridDim.x, warp == 0, cur, pi);
   const int P = pi.P, p = blockIdx.x;
-  if (p >= P) return;
   const long long pstart = pi.pstart, pend = pi.pend;
-  const int len = (int)(pend - pstart);
-  if (len <= 0) return;
+  const int len = p < P ? (int)(pend - pstart) : 0;
+  // A CTA without work still waits for the kernel before it (in inline-plan mode its
+  // wait comes below), so no launch after this grid on the stream can pass the append.
+  if (len <= 0) {
+    if (a.inline_plan) grid_dep_wait();
+    return;
+  }
   // The setup above reads only this call's inputs; the cache and the K tail may still be
   // being written by the kernel before this one on the stream (the quantize-on-append),
   // so every thread waits for it here, with the piece's first block-table line on its way.
@@ -811,6 +816,7 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
                                                const int32_t* tail_seq, int n_tok, uint8_t* cache, void* k_tail,
                                                int tail_rows, int num_blocks, int block_size, int n_kv,
                                                int head_dim, int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_kv_quant_append_int4");
   if (n_tok < 0 || num_blocks < 0 || n_kv <= 0 || tail_rows < 0) return PKV_EINVAL;
   if (pkv_int4_record_bytes(block_size, head_dim) == 0) return PKV_EINVAL;
   if (n_tok == 0) return PKV_OK;
@@ -923,6 +929,7 @@ extern "C" pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* c
                                                  int n_kv, int head_dim, int block_size, int num_blocks, void* out,
                                                  int out_dtype, void* workspace, size_t workspace_bytes,
                                                  int32_t* err_flag, void* stream) {
+  PKV_NVTX("pkv_paged_decode_attn_int4");
   return decode_int4(q, cache, k_tail, block_tables, max_blocks, context_lens, scale, 0,
                      batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace, workspace_bytes,
                      err_flag, stream);
@@ -935,6 +942,7 @@ extern "C" pkv_status pkv_paged_decode_attn_int4_window(const void* q, const uin
                                                         int block_size, int num_blocks, void* out, int out_dtype,
                                                         void* workspace, size_t workspace_bytes, int32_t* err_flag,
                                                         void* stream) {
+  PKV_NVTX("pkv_paged_decode_attn_int4_window");
   return decode_int4(q, cache, k_tail, block_tables, max_blocks, context_lens, scale, window, batch, n_h, n_kv, head_dim, block_size, num_blocks, out, out_dtype, workspace,
                      workspace_bytes, err_flag, stream);
 }

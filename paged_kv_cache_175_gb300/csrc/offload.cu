@@ -9,6 +9,7 @@
 
 #include "../../include/pkv_bm.h"
 #include "decode_common.cuh"   // record_cuda_error
+#include "nvtx_range.h"
 
 namespace pkv {
 
@@ -72,6 +73,7 @@ using namespace pkv;
 extern "C" pkv_status pkv_copy_blocks(const pkv_block_copy* copies, int n, void* k_pool, void* v_pool,
                                       int num_blocks, void* k_host, void* v_host, int host_blocks,
                                       size_t block_bytes, void* stream) {
+  PKV_NVTX("pkv_copy_blocks");
   if (n < 0 || num_blocks < 0 || host_blocks < 0 || block_bytes == 0 || block_bytes % 16) return PKV_EINVAL;
   if (n == 0) return PKV_OK;
   if (!copies || !k_pool || !v_pool || !k_host || !v_host) return PKV_EINVAL;

@@ -58,3 +58,21 @@ def test_binding_refuses_cpu_tensors(built):
     with pytest.raises(pkv.PkvError):
         pkv.kv_append(k, k, torch.zeros(1, dtype=torch.int64), torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16),
                       torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16))
+
+
+def test_layer_window_is_the_list_repeated_over_the_layers(built):
+    # "KV 캐시 시스템 (KV Cache System)", section "어텐션 윈도우 크기": the page's own
+    # examples, one window for every layer and [4096, 256] alternating over six layers
+    import oracle
+    assert pkv.layer_windows([4096], 4) == [4096] * 4
+    assert pkv.layer_windows([4096, 256], 6) == [4096, 256, 4096, 256, 4096, 256]
+    for lst, n in (([4096, 256, 128], 4), ([7], 1), ([1, 2, 3, 4, 5], 12)):
+        assert pkv.layer_windows(lst, n) == oracle.layer_windows(lst, n)
+    for bad in ([], [0], [4096, -1]):
+        with pytest.raises(ValueError):
+            pkv.layer_windows(bad, 3)
+    import ctypes
+    assert pkv.lib().pkv_layer_window(None, 2, 0) == -1
+    w = (ctypes.c_int32 * 2)(8, 16)
+    assert pkv.lib().pkv_layer_window(w, 2, -1) == -1
+    assert pkv.lib().pkv_layer_window(w, 2, 5) == 16
