@@ -86,3 +86,26 @@ def test_shape_beyond_the_static_scratch_is_rejected(library):
     st = library.pkv_paged_decode_attn_noalloc(None, None, None, None, 1, None, ctypes.c_float(0.1), 4096, 64, 1,
                                                128, 16, 1, None, 0, None, None)
     assert st == -2 and library.pkv_status_str(st) == b"size out of range"
+
+
+def test_python_wrapper_against_the_oracle(library):
+    # the tiny workload through pkv.paged_decode_attn_noalloc, checked against the fp64
+    # oracle with the bars of the other attention tests (bf16 and fp32 output)
+    import oracle
+    from gpu_common import check_attention
+    w = workloads.make("tiny", 0)
+    kp, vp = workloads.pools_bf16(w, 0, DEV)
+    q = workloads.queries(w, 0, DEV)
+    ref = oracle.paged_decode_attention(f64(q), f64(kp), f64(vp), w.block_tables, w.context_lens, w.scale,
+                                        w.block_size)
+    for od in (torch.bfloat16, torch.float32):
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = pkv.paged_decode_attn_noalloc(q, kp, vp, torch.as_tensor(w.block_tables, device=DEV),
+                                            torch.as_tensor(w.context_lens, device=DEV), w.scale, out_dtype=od,
+                                            err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        check_attention(out, ref, f"noalloc tiny {od}")
+    with pytest.raises(AssertionError):                  # int64 tables are refused, not misread
+        pkv.paged_decode_attn_noalloc(q, kp, vp, torch.as_tensor(w.block_tables, device=DEV).long(),
+                                      torch.as_tensor(w.context_lens, device=DEV), w.scale)
