@@ -17,9 +17,10 @@ Readings of what the page leaves open (each one is also a line of the design not
   (3) s16 = fp16(s32), m16 = fp16(lo), both round to nearest even;
   (4) code = clamp(rint_half_even((x - m16) / s16), 0, 15) with float32
       subtract and divide; a group with s16 == 0 gets code 0 everywhere;
-  (5) x^ = fp16(code * s16 + m16): the exact value rounded once to fp16 (nearest
-      even).  The page fixes no precision for the reconstruction; with an fp16 scale
-      and min the reading taken is that a dequantized cache value is an fp16 number.
+  (5) x^ = code * s16 + m16, the exact value (no rounding).  The page fixes the step
+      size and the codes; the reconstruction is read as its plain definition, code times
+      scale plus minimum, formed exactly (float64 holds it: a 4-bit code times an fp16
+      scale plus an fp16 minimum is a multiple of 2^-24 below 2^21).
 * Group extent.  V: the head_dim channels of one (token, kv head).  K: one
   channel of one (block, kv head) over the block's block_size tokens.
 * Streaming.  A block's per-channel K range is only known once the block is
@@ -74,14 +75,9 @@ def quantize_groups(x) -> tuple:
 
 
 def dequantize(codes, s16, m16):
-    """x^ = fp16(code * s + min) (step 5), returned as float32; s16 / m16 broadcast against codes.
-
-    The sum is formed exactly in float64 (a 4-bit code times an fp16 scale plus an fp16
-    min needs at most 51 bits) and rounded once to fp16.
-    """
-    exact = (np.asarray(codes, dtype=np.float64) * np.asarray(s16, dtype=np.float64)
-             + np.asarray(m16, dtype=np.float64))
-    return exact.astype(np.float16).astype(np.float32)
+    """x^ = code * s + min (step 5), exact, as float64; s16 / m16 broadcast against codes."""
+    return (np.asarray(codes, dtype=np.float64) * np.asarray(s16, dtype=np.float64)
+            + np.asarray(m16, dtype=np.float64))
 
 
 def pack_codes(codes) -> np.ndarray:

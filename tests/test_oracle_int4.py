@@ -78,8 +78,7 @@ def test_dequant_error_bound_random():
         xh = dequantize(codes, s16, m16).astype(np.float64)
         s = float(s16)
         s_true = (float(x.max()) - float(x.min())) / 15
-        bound = (0.5 * s + abs(float(m16) - float(x.min())) + 15 * abs(s - s_true)
-                 + 2.0 ** -11 * np.abs(xh).max() + 1e-6 * np.abs(x).max())
+        bound = 0.5 * s + abs(float(m16) - float(x.min())) + 15 * abs(s - s_true) + 1e-6 * np.abs(x).max()
         assert np.max(np.abs(xh - x)) <= bound
         assert codes.max() <= 15
 
@@ -98,19 +97,26 @@ def test_vectorised_quantizer_equals_the_scalar_one():
             assert s16[i, j].tobytes() == np.float16(s).tobytes() and m16[i, j].tobytes() == np.float16(m).tobytes()
 
 
-def test_dequant_rounds_the_exact_value_once_to_fp16():
-    # code 13, scale 0.0999755859375 (fp16), min -7.3984375 (fp16): the exact value needs more
-    # than 11 bits; the result is the nearest fp16 to it
+def test_dequant_is_the_exact_value():
+    # x^ = code * s + min with nothing rounded: compared with rational arithmetic on values
+    # whose sum needs more bits than fp16 (11) or fp32 (24) carry
     s16, m16 = np.float16(0.1), np.float16(-7.4)
-    exact = Fraction(13) * Fraction(float(s16)) + Fraction(float(m16))
     got = dequantize(np.array([13]), s16, m16)[0]
-    assert np.float16(got) == got
-    assert got == _nearest_fp16(exact)
-    # no double rounding through float32: a value just above an fp16 tie
-    s16, m16 = np.float16(2.0 ** -24), np.float16(1.0)          # 1 + 2^-24 * c
+    assert Fraction(float(got)) == Fraction(13) * Fraction(float(s16)) + Fraction(float(m16))
+    assert np.float16(got) != got                               # not an fp16 number
+    s16, m16 = np.float16(2.0 ** -24), np.float16(1024.0)       # 1024 + c * 2^-24: 35 bits
     for c in range(16):
-        ex = Fraction(1) + c * Fraction(2) ** -24
-        assert dequantize(np.array([c]), s16, m16)[0] == _nearest_fp16(ex)
+        v = dequantize(np.array([c]), s16, m16)[0]
+        assert Fraction(float(v)) == Fraction(1024) + c * Fraction(2) ** -24
+    assert dequantize(np.array([5]), s16, m16)[0] != np.float32(dequantize(np.array([5]), s16, m16)[0])
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 16, 500)
+    ss = rng.standard_normal(500).astype(np.float16) * np.float16(3)
+    ss = np.abs(ss)
+    mm = rng.standard_normal(500).astype(np.float16) * np.float16(20)
+    got = dequantize(codes, ss, mm)
+    for c, a, b, g in zip(codes, ss, mm, got):
+        assert Fraction(float(g)) == int(c) * Fraction(float(a)) + Fraction(float(b))
 
 
 def test_pack_order_explicit_bytes():
