@@ -182,8 +182,7 @@ int pkv_layer_window(const int32_t* windows, int n, int layer);
  *   s32 = (hi - lo) / 15 (fp32, nearest);
  *   s16 = fp16(s32), m16 = fp16(lo) (nearest even);
  *   code = clamp(rint_half_even((x - m16) / s16), 0, 15) (fp32 subtract / divide),
- *   code = 0 when s16 == 0; dequantized x^ = fp16(code * s16 + m16), the exact value
- *   rounded once to fp16.
+ *   code = 0 when s16 == 0; the dequantized value is x^ = code * s16 + m16, exact.
  * Groups: V = the head_dim channels of one (token, kv head); K = one channel of one
  * (block, kv head) over the block's block_size rows.  K rows of a block that is not
  * yet full stay in bf16 in `k_tail`; when a call appends a block's last row, the
@@ -223,13 +222,18 @@ size_t pkv_int4_record_bytes(int block_size, int head_dim);
 
 /*
  * paged_decode_attn_int4 — decode attention over the INT4 cache written by
- * pkv_kv_quant_append_int4.  Full blocks are dequantized in registers (K and V
- * to fp16, x^ = code * s + m); the last, unfinished block of sequence s takes
- * its K rows from k_tail[s] (bf16) and its V rows from the codes.
+ * pkv_kv_quant_append_int4, equal to the attention over the exact x^ = code * s + m
+ * up to fp32 accumulation: no value is dequantized.  Per block, K's per-channel scale is
+ * folded into q (q * s as an fp16 pair, high part + exact residual) against the codes as
+ * exact small integers, and the block's sum of q * min is one more product; V's per-token
+ * scale is folded into the softmax weights (p * s as a bf16 high + low pair) against the
+ * codes, and sum_t p_t * (min_t + 8 s_t) is added per head at the end.  The last,
+ * unfinished block of sequence s takes its K rows from k_tail[s] (bf16) and its V rows
+ * from the codes.
  * Same arguments and output as pkv_paged_decode_attn, with the INT4 cache and the
- * K tail in place of the pools; the batch index is the tail row.  q.k and p.v use fp16
- * tensor-core mma with fp32 accumulation (q converted to fp16 once; p carried as an
- * fp16 high + low pair).  The dequantized values, q and the tail must lie in fp16 range.
+ * K tail in place of the pools; the batch index is the tail row.  q.k uses fp16 and p.v
+ * bf16 tensor-core mma with fp32 accumulation.  q, the tail and every product q_c * s_c
+ * must lie in fp16 range.
  */
 pkv_status pkv_paged_decode_attn_int4(const void* q, const uint8_t* cache, const void* k_tail,
                                       const int32_t* block_tables,

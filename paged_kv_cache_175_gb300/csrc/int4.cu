@@ -254,20 +254,34 @@ __global__ void __launch_bounds__(256) tail_write_kernel(const QuantAppendArgs a
 // its K rows are read from the bf16 tail straight from L2 (the producer prefetches them
 // when it enters the segment), so the ring holds no tail space.
 //
-// S^T = K^ Q^T uses fp16 mma.  The channel order inside a k-step is chosen so each
-// thread's A-fragment rows come from one 16-byte load of a token row: thread t of a quad
-// owns channels [t*D/4, (t+1)*D/4); k-step ks takes word ks/2 and, inside it, channel
-// pairs (0,1),(2,3) or (4,5),(6,7); Q^T (converted to fp16 once per segment part) uses
-// the same order.  Dequantization x^ = fp16(code * s + m) runs on half2 pairs: the code
-// pair is unpacked into 1024 + code by a mask-and-or, 1024 is subtracted (exact), then
-// one fused multiply-add with the pair's (s, m) rounds the exact value once, as the
-// format defines it.
+// No value is dequantized: the scales are folded into the other operand, so the result is
+// the attention over the exact x^ = code * s + min up to fp32 accumulation.
 //
-// O^T = V^T P^T uses fp16 mma with P carried as an fp16 high part plus an fp16 low part.
-// Thread g of the eight row groups owns channels [g*D/8, (g+1)*D/8); a byte of a V code
-// word, permuted together from two token rows, gives a half2 of two tokens of one channel
-// (the even nibble for fragment row g, the odd one for row g+8), scaled by the two
-// tokens' (s, m).
+// S^T = K^ Q^T, fp16 mma.  K^[t][c] = code * s_c + m_c with a per-channel (s, m) per
+// block, so  q . k^_t = sum_c (16 + code_tc) (q_c s_c) + sum_c q_c (m_c - 16 s_c).
+// The A operand is 16 + code, exact in fp16, made from a nibble pair by one shift and one
+// mask-and-or (the code lands in mantissa bits 6..9 under the exponent of 16).  The B
+// operand is q * s, carried as an fp16 high part and the exact residual (q is bf16 and s
+// fp16, so their product has at most 19 significant bits: high + low holds it exactly).
+// The second sum, a constant of the block per head, is one more mma chain with the min
+// row and the scale row of the block as A rows 0 and 1 and q as B; it initialises the
+// score accumulators.  For groups of up to 4 heads the 8-head n-tile carries the high
+// part in columns 0-3 and the low part in columns 4-7, so one mma takes both and one
+// shuffle adds the halves.  The channel order inside a k-step is permuted so each thread's
+// A-fragment rows come from one 16-byte load of a token row: thread t of a quad owns
+// channels [t*D/4, (t+1)*D/4); k-step ks takes word ks/2 and, inside it, channel pairs
+// (0,1),(2,3) or (4,5),(6,7); Q^T uses the same order.
+//
+// O^T = V^T P^T, bf16 mma.  V^[t][c] = code * s_t + m_t with a per-token (s, m), so
+//   sum_t p_t v^_tc = sum_t (code_tc - 8) (p_t s_t) + sum_t p_t (m_t + 8 s_t).
+// The A operand is code - 8, exact in bf16 (mask-and-or into 128 + code, minus 136),
+// centred so the accumulated terms have both signs; the B operand is p * s as a bf16 high
+// + low pair; the second sum is a per-head fp32 scalar that each thread accumulates over
+// its tokens and that is added to every channel at the end.  Thread g of the eight row
+// groups owns channels [g*D/8, (g+1)*D/8); a byte of a V code word, permuted together from
+// two token rows, gives a pair of two tokens of one channel (the even nibble for fragment
+// row g, the odd one for row g+8).  For groups of up to 4 heads the P^T columns 4-7 carry
+// the low part, as for the scores.
 template <int D, int BS>
 struct Int4Tile {
   static constexpr int KC = 0;                              // K codes [BS][D/2]
@@ -283,34 +297,117 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
-__device__ __forceinline__ uint32_t lop_nib(uint32_t x) {   // (x & 0x000f000f) | 0x64006400
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t bits) {   // (x & mask) | bits
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(d) : "r"(x), "r"(0x000f000fu), "r"(0x64006400u));
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(d) : "r"(x), "r"(mask), "r"(bits));
   return d;
 }
-__device__ __forceinline__ uint32_t dq2(uint32_t h1024, uint32_t s2, uint32_t m2) {
-  const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&h1024), __half2half2(__ushort_as_half(0x6400)));
-  const __half2 r = __hfma2(c, *reinterpret_cast<const __half2*>(&s2), *reinterpret_cast<const __half2*>(&m2));
+__device__ __forceinline__ uint32_t xor_and(uint32_t x, uint32_t y, uint32_t mask) {     // (x ^ y) & mask
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(d) : "r"(x), "r"(y), "r"(mask));
+  return d;
+}
+// fp16 pair (16 + code of nibble j, 16 + code of nibble j + 4) of a K code word: the
+// nibbles sit at bits 4j and 16 + 4j and move to mantissa bits 6..9 of each half.
+__device__ __forceinline__ uint32_t k_codes16(uint32_t w, int j) {
+  const uint32_t x = j == 0 ? w << 6 : (j == 1 ? w << 2 : (j == 2 ? w >> 2 : w >> 6));
+  return and_or(x, 0x03c003c0u, 0x4c004c00u);
+}
+// bf16 pair (code - 8) of the nibbles at bits 0..3 and 16..19: 128 + code by a
+// mask-and-or (mantissa bits 0..3 under the exponent of 128), then minus 136, exactly.
+__device__ __forceinline__ uint32_t v_codes8(uint32_t x) {
+  const uint32_t c = and_or(x, 0x000f000fu, 0x43004300u);
+  const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&c),
+                                   __bfloat162bfloat162(__ushort_as_bfloat16(0x4308)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                            *reinterpret_cast<const __half2*>(&c));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) { return pack_f16(bf16_lo(w), bf16_hi(w)); }
-// Keep the halves of a pair of rows (t, t + 1) that lie in [lead, ntok); zero the others.
-__device__ __forceinline__ uint32_t mask_pair_h(uint32_t b, int t, int lead, int ntok) {
-  return b & ((t < ntok && t >= lead ? 0x0000ffffu : 0u) | (t + 1 < ntok && t + 1 >= lead ? 0xffff0000u : 0u));
-}
+__device__ __forceinline__ float h_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
+__device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
-// TB cache records (blocks) per ring stage.
+// TB cache records (blocks) per ring stage; a zero line after the barriers feeds the A rows
+// of the bias product that carry nothing.
 template <int D, int BS, int TB>
 __host__ __device__ constexpr size_t int4_smem_bytes(int stages) {
-  return 128 + (size_t)stages * (TB * Int4Tile<D, BS>::STAGE + 16 + 16);
+  return 128 + (size_t)stages * (TB * Int4Tile<D, BS>::STAGE + 16 + 16) + 2 * D;
 }
 
+// softmax_tile plus the per-head correction sums of the V fold, rescaled with l and O when
+// the running offset rises.
+template <int TT, int NH, int MD>
+__device__ __forceinline__ void softmax_tile_c(float (&sc)[TT][NH][4], float (&m)[NH][2], float (&l)[NH][2],
+                                               float (&c)[NH][2], float (&o)[MD][NH][4], int gid, int ntok,
+                                               int lead, float scale_log2) {
+  bool over = false;
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int tok = t * 16 + gid + 8 * r;
+          float x = sc[t][nh][2 * r + e] * scale_log2;
+          if (tok >= ntok || tok < lead) x = -INFINITY;
+          sc[t][nh][2 * r + e] = x;
+          over |= x > m[nh][e] + kLazyMax;
+        }
+  if (__any_sync(FULL_MASK, over)) {
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) {
+      float al[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) mx = fmaxf(mx, fmaxf(sc[t][nh][e], sc[t][nh][2 + e]));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+        const float mn = fmaxf(m[nh][e], mx);
+        al[e] = ex2(m[nh][e] - mn);
+        m[nh][e] = mn;
+        l[nh][e] *= al[e];
+        c[nh][e] *= al[e];
+      }
+#pragma unroll
+      for (int md = 0; md < MD; ++md) {
+        o[md][nh][0] *= al[0]; o[md][nh][1] *= al[1];
+        o[md][nh][2] *= al[0]; o[md][nh][3] *= al[1];
+      }
+    }
+  }
+#pragma unroll
+  for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float rs = 0.f;
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float pv = ex2(sc[t][nh][2 * r + e] - m[nh][e]);
+          sc[t][nh][2 * r + e] = pv;
+          rs += pv;
+        }
+      l[nh][e] += rs;
+    }
+}
 // TB = 2: a stage holds two consecutive blocks of one segment when the piece has them
 // (32 token rows per pass at block size 16: the per-stage loop, barrier, producer and
-// softmax work is shared by twice the tokens).  Single-warp CTAs are bounded to 12 per SM
-// with two-block stages (170 registers) and 16 per SM with one-block stages at block size
-// 16 (128 registers).
-template <int D, int BS, int NH, int MT, int TB>
+// softmax work is shared by twice the tokens).  COMB: groups of up to 4 heads, high and
+// low parts of the folded operands in the two halves of one 8-head n-tile.
+template <int D, int BS, int NH, int MT, int TB, bool COMB>
 __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 && NH == 1 ? 16 : 0))
     decode_int4_kernel(const DecodeArgs a) {
   using T = Int4Tile<D, BS>;
@@ -333,6 +430,8 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
   __shared__ volatile int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3, gid = lane >> 2;
 
+  uint32_t* zline = reinterpret_cast<uint32_t*>(empty + S);     // 2 * D zero bytes
+  for (int i = threadIdx.x; i < D / 2; i += MT * 32) zline[i] = 0u;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < S; ++i) {
@@ -468,19 +567,19 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
   };
 
   // ---------------- consumer state (warp w: local heads [w*HW, (w+1)*HW)) ----------------
-  // Token-major tiles as in the bf16 kernel.  K^ is the A operand (tokens x channels); its
-  // channel order inside a k-step follows the code words: thread tig owns channels
-  // [tig*CB, (tig+1)*CB); k-step ks takes word ks/2 and, in it, the pairs (0,1),(2,3) or
-  // (4,5),(6,7) -- Q^T's B fragments use the same order.  V^T is the A operand of the
-  // second product (channels x tokens): thread gid owns channels [gid*CV, (gid+1)*CV);
-  // byte k of code word w of two token rows gives the m-tile 4w+k rows gid (even nibble)
-  // and gid+8 (odd nibble).
+  // Token-major tiles as in the bf16 kernel.  qb: q in fp16 (exact for bf16 values in fp16
+  // range) as QK B fragments in the permuted channel order; with COMB, column n holds head
+  // n % 4 (columns 4-7 repeat 0-3 and carry the low parts of the folded products).
   uint32_t qb[KS][NH][2];
   float o[MD][NH][4];
-  float m[NH][2], l[NH][2];
+  float m[NH][2], l[NH][2], cs[NH][2];        // running offset, sum, V-fold correction
   const int hw0 = warp * HW;
   const int cb = tig * CB;           // first K channel of this thread
   const int cv = gid * CV;           // first V channel of this thread
+  // A rows of the bias product: row 0 the block's K min row, row 1 its K scale row, the
+  // other rows read the zero line
+  const int xrow = gid == 0 ? T::KM + 2 * D : (gid == 1 ? T::KM : -1);
+  const uint32_t lo_lane = COMB && gid >= 4 ? 0xffffffffu : 0u;  // columns 4-7: low parts
 
   if (warp == 0)
     for (int k = 0; k < S && pj < len; ++k) issue();
@@ -502,7 +601,7 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
     if (flags & F_FIRST) {
 #pragma unroll
       for (int nh = 0; nh < NH; ++nh) {
-        const int hl = hw0 + nh * 8 + gid;
+        const int hl = COMB ? (gid & 3) : hw0 + nh * 8 + gid;
         const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q) + (qrow0 + hl) * (D / 2);
         const bool ok = hl < a.G;
 #pragma unroll
@@ -513,6 +612,7 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
         }
         m[nh][0] = m[nh][1] = -INFINITY;
         l[nh][0] = l[nh][1] = 0.f;
+        cs[nh][0] = cs[nh][1] = 0.f;
 #pragma unroll
         for (int md = 0; md < MD; ++md) o[md][nh][0] = o[md][nh][1] = o[md][nh][2] = o[md][nh][3] = 0.f;
       }
@@ -525,7 +625,7 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
       // its rows stop short of the block
       const int tail_rec = ntok < nblk * BS ? nblk - 1 : -1;   // (at most one record per stage)
       const bool masked = ntok < TT * 16 || lead > 0;
-      // ---- S^T = K^ Q^T (fp16 in, fp32 accumulate; even / odd k-steps in two accumulators) ----
+      // ---- S^T = K^ Q^T (fp16 in, fp32 accumulate; two accumulators per tile) ----
       float sc[TT][NH][4], sx[TT][NH][4];
 #pragma unroll
       for (int t = 0; t < TT; ++t)
@@ -538,47 +638,96 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
         if (rec >= nblk) continue;
         const uint8_t* st = stg + rec * T::STAGE;
         if (rec != tail_rec) {
-          uint32_t s2[CB / 2], m2[CB / 2];                        // (s, m) of channel pairs cb + 2k
-          const uint4* kms = reinterpret_cast<const uint4*>(st + T::KM + cb * 2);
-          const uint4* kmm = reinterpret_cast<const uint4*>(st + T::KM + 2 * D + cb * 2);
+          uint32_t s2[CB / 2], x2[CB / 2];             // scale pairs of channels cb + 2k; bias A rows
+          {
+            const uint4* ks4 = reinterpret_cast<const uint4*>(st + T::KM + cb * 2);
+            const uint4* xs4 = reinterpret_cast<const uint4*>(
+                (xrow >= 0 ? st + xrow : reinterpret_cast<const uint8_t*>(zline)) + cb * 2);
 #pragma unroll
-          for (int k4 = 0; k4 < CB / 8; ++k4) {
-            const uint4 a4 = kms[k4], b4 = kmm[k4];
-            s2[4 * k4] = a4.x; s2[4 * k4 + 1] = a4.y; s2[4 * k4 + 2] = a4.z; s2[4 * k4 + 3] = a4.w;
-            m2[4 * k4] = b4.x; m2[4 * k4 + 1] = b4.y; m2[4 * k4 + 2] = b4.z; m2[4 * k4 + 3] = b4.w;
+            for (int k4 = 0; k4 < CB / 8; ++k4) {
+              const uint4 a4 = ks4[k4], b4 = xs4[k4];
+              s2[4 * k4] = a4.x; s2[4 * k4 + 1] = a4.y; s2[4 * k4 + 2] = a4.z; s2[4 * k4 + 3] = a4.w;
+              x2[4 * k4] = b4.x; x2[4 * k4 + 1] = b4.y; x2[4 * k4 + 2] = b4.z; x2[4 * k4 + 3] = b4.w;
+            }
           }
+          // bias of each head column: sum_c q_c m_c - 16 sum_c q_c s_c (rows 0 and 1 of one
+          // mma chain), the starting value of the block's score accumulators
+#pragma unroll
+          for (int nh = 0; nh < NH; ++nh) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              const int pr = 4 * (ks >> 1) + 2 * (ks & 1);
+              const uint32_t xa[4] = {x2[pr], 0u, x2[pr + 1], 0u};
+              mma_f16(d, xa, qb[ks][nh][0], qb[ks][nh][1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float bm = __shfl_sync(FULL_MASK, d[e], tig);
+              const float bsq = __shfl_sync(FULL_MASK, d[e], 4 + tig);
+              const float bias = (COMB && tig >= 2) ? 0.f : fmaf(-16.f, bsq, bm);
+#pragma unroll
+              for (int tt = 0; tt < TPB; ++tt) {
+                sc[rec * TPB + tt][nh][e] = bias;
+                sc[rec * TPB + tt][nh][2 + e] = bias;
+              }
+            }
+          }
+          uint32_t w0[TPB][KW], w1[TPB][KW];                       // code words of rows gid, gid+8
 #pragma unroll
           for (int tt = 0; tt < TPB; ++tt) {
-            const int t = rec * TPB + tt;
-            uint32_t w0[KW], w1[KW];                              // code words of rows gid, gid+8
             const uint8_t* q0 = st + T::KC + (tt * 16 + gid) * (D / 2) + tig * (D / 8);
             const uint8_t* q1 = q0 + 8 * (D / 2);
             if constexpr (KW == 4) {
               const uint4 x = *reinterpret_cast<const uint4*>(q0), y = *reinterpret_cast<const uint4*>(q1);
-              w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
-              w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
+              w0[tt][0] = x.x; w0[tt][1] = x.y; w0[tt][2] = x.z; w0[tt][3] = x.w;
+              w1[tt][0] = y.x; w1[tt][1] = y.y; w1[tt][2] = y.z; w1[tt][3] = y.w;
             } else {
               const uint2 x = *reinterpret_cast<const uint2*>(q0), y = *reinterpret_cast<const uint2*>(q1);
-              w0[0] = x.x; w0[1] = x.y;
-              w1[0] = y.x; w1[1] = y.y;
+              w0[tt][0] = x.x; w0[tt][1] = x.y;
+              w1[tt][0] = y.x; w1[tt][1] = y.y;
             }
+          }
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-              const int w = ks >> 1, hs = 2 * (ks & 1), pr = 4 * w + hs;
+          for (int ks = 0; ks < KS; ++ks) {
+            const int w = ks >> 1, j0 = 2 * (ks & 1), pr = 4 * w + j0;
+            // B: q * s, high part and exact low part (COMB: the low part in columns 4-7)
+            uint32_t bh[NH][2], bl[NH][2];
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t hi = hmul2_u(qb[ks][nh][j], s2[pr + j]);
+                if (COMB) {
+                  bh[nh][j] = hfma2_u(qb[ks][nh][j], s2[pr + j], xor_and(hi, 0x80008000u, lo_lane));
+                } else {
+                  bh[nh][j] = hi;
+                  bl[nh][j] = hfma2_u(qb[ks][nh][j], s2[pr + j], hi ^ 0x80008000u);
+                }
+              }
+#pragma unroll
+            for (int tt = 0; tt < TPB; ++tt) {
+              const int t = rec * TPB + tt;
               uint32_t ka[4];
-              ka[0] = dq2(lop_nib(w0[w] >> (4 * hs)), s2[pr], m2[pr]);
-              ka[1] = dq2(lop_nib(w1[w] >> (4 * hs)), s2[pr], m2[pr]);
-              ka[2] = dq2(lop_nib(w0[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
-              ka[3] = dq2(lop_nib(w1[w] >> (4 * hs + 4)), s2[pr + 1], m2[pr + 1]);
+              ka[0] = k_codes16(w0[tt][w], j0);
+              ka[1] = k_codes16(w1[tt][w], j0);
+              ka[2] = k_codes16(w0[tt][w], j0 + 1);
+              ka[3] = k_codes16(w1[tt][w], j0 + 1);
 #pragma unroll
               for (int nh = 0; nh < NH; ++nh) {
-                if (ks & 1) mma_f16(sx[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
-                else mma_f16(sc[t][nh], ka, qb[ks][nh][0], qb[ks][nh][1]);
+                if (COMB) {
+                  if (ks & 1) mma_f16(sx[t][nh], ka, bh[nh][0], bh[nh][1]);
+                  else mma_f16(sc[t][nh], ka, bh[nh][0], bh[nh][1]);
+                } else {
+                  mma_f16(sc[t][nh], ka, bh[nh][0], bh[nh][1]);
+                  mma_f16(sx[t][nh], ka, bl[nh][0], bl[nh][1]);
+                }
               }
             }
           }
         } else {
-          // unfinished block: K rows from the bf16 tail in global memory (prefetched to L2)
+          // unfinished block: K rows from the bf16 tail in global memory (prefetched to L2),
+          // converted to fp16 (exact in range), against q itself
           const uint4* tl = reinterpret_cast<const uint4*>(a.k_tail + ((size_t)s * a.n_kv + g) * BS * D);
 #pragma unroll
           for (int tt = 0; tt < TPB; ++tt) {
@@ -610,43 +759,67 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
         }
       }
 #pragma unroll
-      for (int t = 0; t < TT; ++t)
+      for (int t = 0; t < TT; ++t) {
+        const bool comb_tile = COMB && t / TPB < nblk && t / TPB != tail_rec;
 #pragma unroll
         for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sc[t][nh][i] += sx[t][nh][i];
-      softmax_tile<TT, NH, MD>(sc, m, l, o, gid, ntok, lead, a.scale_log2);
-      // ---- O^T += V^T P^T (fp16, P as high + low) ----
+          for (int i = 0; i < 4; ++i) {
+            float x = sc[t][nh][i] + sx[t][nh][i];
+            // COMB: the high-part sums (columns 0-3) and the low-part sums (4-7) of the same
+            // heads, added in both halves (the tail block's two halves already hold the score)
+            if (COMB) {
+              const float y = __shfl_xor_sync(FULL_MASK, x, 2);
+              if (comb_tile) x += y;
+            }
+            sc[t][nh][i] = x;
+          }
+      }
+      softmax_tile_c<TT, NH, MD>(sc, m, l, cs, o, gid, ntok, lead, a.scale_log2);
+      // ---- O^T += V^T P'^T (bf16, P' = p * s_t as high + low) ----
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
         const int rec = t / TPB, r0 = (t % TPB) * 16;             // record, first row in it
         if (rec >= nblk) continue;
         const uint8_t* st = stg + rec * T::STAGE;
         const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + T::VM);
+        // (s, m) of this thread's token rows gid and gid + 8; rows outside [lead, ntok) get
+        // 0 and 0 (their p is 0 and their metadata may never have been written)
+        uint32_t u0 = vm[r0 + gid], u1 = vm[r0 + gid + 8];
+        if (masked) {
+          const int k0 = t * 16 + gid, k1 = k0 + 8;
+          if (k0 >= ntok || k0 < lead) u0 = 0u;
+          if (k1 >= ntok || k1 < lead) u1 = 0u;
+        }
+        const float sA = h_lo(u0), sB = h_lo(u1);
+        const float cA = fmaf(8.f, sA, h_hi(u0)), cB = fmaf(8.f, sB, h_hi(u1));   // min + 8 s
         uint32_t bh[NH][2], bl[NH][2];
 #pragma unroll
-        for (int nh = 0; nh < NH; ++nh)
+        for (int nh = 0; nh < NH; ++nh) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float p0 = sc[t][nh][e], p1 = sc[t][nh][2 + e];
+            cs[nh][e] = fmaf(p0, cA, fmaf(p1, cB, cs[nh][e]));
+            sc[t][nh][e] = p0 * sA;
+            sc[t][nh][2 + e] = p1 * sB;
+          }
+          // B fragments of P'^T (k = token, n = head): the S^T rows of tokens 0-7 / 8-15 of
+          // the tile, packed per head pair and transposed
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const float x = sc[t][nh][2 * r], y = sc[t][nh][2 * r + 1];
-            const uint32_t hi = pack_f16(x, y);
-            const __half2 h = *reinterpret_cast<const __half2*>(&hi);
-            const uint32_t lo = pack_f16(x - __low2float(h), y - __high2float(h));
-            bh[nh][r] = movmatrix_t(hi);
-            bl[nh][r] = movmatrix_t(lo);
+            const uint32_t hi = pack_bf16(x, y);
+            const uint32_t lo = pack_bf16(x - bf16_lo(hi), y - bf16_hi(hi));
+            if (COMB) {
+              const uint32_t lo_of_pair = __shfl_xor_sync(FULL_MASK, lo, 2);
+              bh[nh][r] = movmatrix_t(tig < 2 ? hi : lo_of_pair);
+            } else {
+              bh[nh][r] = movmatrix_t(hi);
+              bl[nh][r] = movmatrix_t(lo);
+            }
           }
-        const int t0 = r0 + 2 * tig;                 // a0/a1: record rows t0, t0+1; a2/a3: +8
-        const int u0 = t * 16 + 2 * tig;             // the same rows counted in the stage
-        uint32_t sA = prmt(vm[t0], vm[t0 + 1], 0x5410), mA = prmt(vm[t0], vm[t0 + 1], 0x7632);
-        uint32_t sB = prmt(vm[t0 + 8], vm[t0 + 9], 0x5410), mB = prmt(vm[t0 + 8], vm[t0 + 9], 0x7632);
-        if (masked) {
-          // rows outside [lead, ntok) get scale = min = 0, so their V^ is exactly 0 whatever
-          // their codes (rows past ntok were never written)
-          sA = mask_pair_h(sA, u0, lead, ntok);
-          mA = mask_pair_h(mA, u0, lead, ntok);
-          sB = mask_pair_h(sB, u0 + 8, lead, ntok);
-          mB = mask_pair_h(mB, u0 + 8, lead, ntok);
         }
+        const int t0 = r0 + 2 * tig;                 // a0/a1: record rows t0, t0+1; a2/a3: +8
         const uint8_t* vc = st + T::VC + cv / 2;
 #pragma unroll
         for (int w = 0; w < VW; ++w) {
@@ -656,17 +829,19 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
           const uint32_t rd = *reinterpret_cast<const uint32_t*>(vc + (size_t)(t0 + 9) * (D / 2) + 4 * w);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
+            // byte k of the two rows' words: [a_k, a_k, b_k, b_k]; the even nibble is fragment
+            // row gid, the odd one row gid + 8
             const uint32_t sel = (uint32_t)k | ((uint32_t)k << 4) | ((uint32_t)(4 + k) << 8) | ((uint32_t)(4 + k) << 12);
             const uint32_t pab = prmt(ra, rb, sel), pcd = prmt(rc, rd, sel);
             uint32_t va[4];
-            va[0] = dq2(lop_nib(pab), sA, mA);                   // row gid   (even nibble), tokens t0, t0+1
-            va[1] = dq2(lop_nib(pab >> 4), sA, mA);              // row gid+8 (odd nibble)
-            va[2] = dq2(lop_nib(pcd), sB, mB);                   // row gid,   tokens t0+8, t0+9
-            va[3] = dq2(lop_nib(pcd >> 4), sB, mB);
+            va[0] = v_codes8(pab);
+            va[1] = v_codes8(pab >> 4);
+            va[2] = v_codes8(pcd);
+            va[3] = v_codes8(pcd >> 4);
 #pragma unroll
             for (int nh = 0; nh < NH; ++nh) {
-              mma_f16(o[4 * w + k][nh], va, bh[nh][0], bh[nh][1]);
-              mma_f16(o[4 * w + k][nh], va, bl[nh][0], bl[nh][1]);
+              mma_bf16(o[4 * w + k][nh], va, bh[nh][0], bh[nh][1]);
+              if (!COMB) mma_bf16(o[4 * w + k][nh], va, bl[nh][0], bl[nh][1]);
             }
           }
         }
@@ -674,17 +849,26 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
     }
 
     if (flags & F_LAST) {
-      float L[NH][2];
+      float L[NH][2], C[NH][2];
 #pragma unroll
       for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float x = l[nh][e];
-          x += __shfl_xor_sync(FULL_MASK, x, 4);
-          x += __shfl_xor_sync(FULL_MASK, x, 8);
-          x += __shfl_xor_sync(FULL_MASK, x, 16);
+          float x = l[nh][e], y = cs[nh][e];
+#pragma unroll
+          for (int msk = 4; msk < 32; msk <<= 1) {
+            x += __shfl_xor_sync(FULL_MASK, x, msk);
+            y += __shfl_xor_sync(FULL_MASK, y, msk);
+          }
           L[nh][e] = x;
+          C[nh][e] = y;
         }
+      if (COMB) {                     // the high-part and low-part sums of O, added in both halves
+#pragma unroll
+        for (int md = 0; md < MD; ++md)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[md][0][i] += __shfl_xor_sync(FULL_MASK, o[md][0][i], 2);
+      }
       const bool whole = flags & F_WHOLE;
       const long long part = (long long)s * a.n_kv + g + p;
 #pragma unroll
@@ -694,6 +878,7 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
           const int hl = hw0 + nh * 8 + 2 * tig + e;
           if (hl >= a.G) continue;
           const float inv = whole ? (L[nh][e] > 0.f ? 1.f / L[nh][e] : 0.f) : 1.f;
+          const float c = C[nh][e];
           // m-tile md rows gid / gid+8 hold channel cv + 8*(md/4) + channel_of(2*(md%4) + 0 / 1)
           if (whole) {
             const size_t base = (qrow0 + hl) * D + cv;
@@ -702,20 +887,20 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
               const int c0 = 8 * (md >> 2) + channel_of(2 * (md & 3)), c1 = 8 * (md >> 2) + channel_of(2 * (md & 3) + 1);
               if (a.out_f32) {
                 float* out = reinterpret_cast<float*>(a.out) + base;
-                out[c0] = o[md][nh][e] * inv;
-                out[c1] = o[md][nh][2 + e] * inv;
+                out[c0] = (o[md][nh][e] + c) * inv;
+                out[c1] = (o[md][nh][2 + e] + c) * inv;
               } else {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + base;
-                out[c0] = __float2bfloat16_rn(o[md][nh][e] * inv);
-                out[c1] = __float2bfloat16_rn(o[md][nh][2 + e] * inv);
+                out[c0] = __float2bfloat16_rn((o[md][nh][e] + c) * inv);
+                out[c1] = __float2bfloat16_rn((o[md][nh][2 + e] + c) * inv);
               }
             }
           } else {
             float* wo = a.ws_o + ((size_t)part * a.G + hl) * D + cv;
 #pragma unroll
             for (int md = 0; md < MD; ++md) {
-              wo[8 * (md >> 2) + channel_of(2 * (md & 3))] = o[md][nh][e];
-              wo[8 * (md >> 2) + channel_of(2 * (md & 3) + 1)] = o[md][nh][2 + e];
+              wo[8 * (md >> 2) + channel_of(2 * (md & 3))] = o[md][nh][e] + c;
+              wo[8 * (md >> 2) + channel_of(2 * (md & 3) + 1)] = o[md][nh][2 + e] + c;
             }
             if (gid == 0)
               *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hl) * 2) = make_float2(m[nh][e], L[nh][e]);
@@ -739,7 +924,6 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
       if (!mbar_wait(&full[j % S], (j / S) & 1)) break;
   }
 }
-
 // ---------------------------------------------------------------------------------------------
 struct Int4Variant {
   const void* fn;
@@ -749,10 +933,10 @@ struct Int4Variant {
   int P;
 };
 
-template <int D, int BS, int NH, int MT, int TB>
+template <int D, int BS, int NH, int MT, int TB, bool COMB>
 static Int4Variant make_int4_variant() {
   Int4Variant v;
-  v.fn = (const void*)decode_int4_kernel<D, BS, NH, MT, TB>;
+  v.fn = (const void*)decode_int4_kernel<D, BS, NH, MT, TB, COMB>;
   v.stages = ring_stages(TB * Int4Tile<D, BS>::STAGE, BS == 16 ? 11264 : 16384, "PKV_STAGES_INT4");
   v.smem = int4_smem_bytes<D, BS, TB>(v.stages);
   v.warps = MT;
@@ -760,20 +944,25 @@ static Int4Variant make_int4_variant() {
   return v;
 }
 
-static Int4Variant* lookup_int4(int D, int BS, int tiling) {
+// Kernel variant of a group of G heads: 0 = up to 4 heads (high and low parts in one n-tile),
+// 1 = up to 8, 2 = up to 16, 3 = up to 32 (two warps), 4 = up to 64 (four warps).
+static int int4_variant_index(int G) { return G <= 4 ? 0 : head_tiling(G) + 1; }
+
+static Int4Variant* lookup_int4(int D, int BS, int vi) {
   static std::mutex mu;
-  static Int4Variant table[2][3][4];
-  static bool ready[2][3][4] = {};
-  const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2), ti = tiling;
+  static Int4Variant table[2][3][5];
+  static bool ready[2][3][5] = {};
+  const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2);
   std::lock_guard<std::mutex> lock(mu);
-  Int4Variant& v = table[di][bi][ti];
-  if (!ready[di][bi][ti]) {
-#define PKV_V(d, b)                                               \
-  if (D == d && BS == b) {                                        \
-    if (ti == 0) v = make_int4_variant<d, b, 1, 1, b == 16 ? 2 : 1>(); \
-    else if (ti == 1) v = make_int4_variant<d, b, 2, 1, 1>();     \
-    else if (ti == 2) v = make_int4_variant<d, b, 2, 2, 1>();     \
-    else v = make_int4_variant<d, b, 2, 4, 1>();                  \
+  Int4Variant& v = table[di][bi][vi];
+  if (!ready[di][bi][vi]) {
+#define PKV_V(d, b)                                                          \
+  if (D == d && BS == b) {                                                   \
+    if (vi == 0) v = make_int4_variant<d, b, 1, 1, b == 16 ? 2 : 1, true>(); \
+    else if (vi == 1) v = make_int4_variant<d, b, 1, 1, b == 16 ? 2 : 1, false>(); \
+    else if (vi == 2) v = make_int4_variant<d, b, 2, 1, 1, false>();        \
+    else if (vi == 3) v = make_int4_variant<d, b, 2, 2, 1, false>();        \
+    else v = make_int4_variant<d, b, 2, 4, 1, false>();                     \
   }
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
@@ -783,13 +972,13 @@ static Int4Variant* lookup_int4(int D, int BS, int tiling) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.warps * 32, v.smem) != cudaSuccess || occ < 1)
       return nullptr;
     v.P = device_sm_count() * occ;
-    ready[di][bi][ti] = true;
+    ready[di][bi][vi] = true;
   }
   return &v;
 }
 
 int int4_pieces(int D, int BS, int G) {
-  Int4Variant* v = lookup_int4(D, BS, head_tiling(G));
+  Int4Variant* v = lookup_int4(D, BS, int4_variant_index(G));
   return v ? v->P : 0;
 }
 
@@ -874,7 +1063,7 @@ static pkv_status decode_int4(const void* q, const uint8_t* cache, const void* k
     return PKV_EINVAL;
   if ((long long)max_blocks * block_size > 0x7fffffffLL) return PKV_ERANGE;
   const int G = n_h / n_kv;
-  Int4Variant* vv = lookup_int4(head_dim, block_size, head_tiling(G));
+  Int4Variant* vv = lookup_int4(head_dim, block_size, int4_variant_index(G));
   if (!vv) {
     record_cuda_error(cudaGetLastError());
     return PKV_ECUDA;

@@ -148,18 +148,26 @@ def test_full_size_sampled(name):
     q = workloads.queries(w, 0, DEV)
     out = pkv.paged_decode_attn_int4(q, cache, torch.as_tensor(w.block_tables, device=DEV),
                                      torch.as_tensor(w.context_lens, device=DEV), w.scale, err=err)
+    out32 = pkv.paged_decode_attn_int4(q, cache, torch.as_tensor(w.block_tables, device=DEV),
+                                       torch.as_tensor(w.context_lens, device=DEV), w.scale,
+                                       out_dtype=torch.float32, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    s = int(np.argmin(w.context_lens))                           # shortest history: quickest oracle
-    phys, cbt, cctx = compact(w.block_tables, w.context_lens, [s], BS)
-    ref = oracle.Int4Cache(len(phys), w.n_kv, BS, w.head_dim, 1)
-    pos = np.arange(int(w.context_lens[s]))
-    ref.append(f64(hist[s][0]), f64(hist[s][1]), cbt[0, pos // BS].astype(np.int64) * BS + pos % BS,
-               np.zeros(len(pos), np.int32))
-    idx = torch.as_tensor(phys, device=DEV)
-    assert np.array_equal(cache.k_codes[idx].cpu().numpy(), ref.k_codes)
-    assert np.array_equal(cache.v_codes[idx].cpu().numpy(), ref.v_codes)
-    assert cache.k_meta[idx].cpu().numpy().tobytes() == ref.k_meta.tobytes()
-    assert cache.v_meta[idx].cpu().numpy().tobytes() == ref.v_meta.tobytes()
-    refo = oracle.paged_decode_attention_int4(f64(q[s:s + 1]), ref, cbt, cctx, w.scale)
-    check_attention(out[s:s + 1], refo, name, min_exact=0.95)
+    # the shortest, the median and the longest history: the longest is cut across the most
+    # pieces (every split merge), and each ends in an unfinished block read from the tail
+    order = np.argsort(w.context_lens, kind="stable")
+    for s in (int(order[0]), int(order[len(order) // 2]), int(order[-1])):
+        phys, cbt, cctx = compact(w.block_tables, w.context_lens, [s], BS)
+        ref = oracle.Int4Cache(len(phys), w.n_kv, BS, w.head_dim, 1)
+        pos = np.arange(int(w.context_lens[s]))
+        ref.append(f64(hist[s][0]), f64(hist[s][1]), cbt[0, pos // BS].astype(np.int64) * BS + pos % BS,
+                   np.zeros(len(pos), np.int32))
+        idx = torch.as_tensor(phys, device=DEV)
+        assert np.array_equal(cache.k_codes[idx].cpu().numpy(), ref.k_codes)
+        assert np.array_equal(cache.v_codes[idx].cpu().numpy(), ref.v_codes)
+        assert cache.k_meta[idx].cpu().numpy().tobytes() == ref.k_meta.tobytes()
+        assert cache.v_meta[idx].cpu().numpy().tobytes() == ref.v_meta.tobytes()
+        refo = oracle.paged_decode_attention_int4(f64(q[s:s + 1]), ref, cbt, cctx, w.scale)
+        check_attention(out[s:s + 1], refo, f"{name} seq {s} ctx {int(w.context_lens[s])}", min_exact=0.95)
+        check_attention(out32[s:s + 1], refo, f"{name} seq {s} fp32",
+                        f32_bars=(BAR_INT4_F32_MAXABS, BAR_INT4_F32_RELL2))
