@@ -191,10 +191,17 @@ def bench_probes(dev, stream, nbytes=4 << 30, K=10, W=3):
             "bytes": nbytes, "best_of": K, "launches": 2 * (K + W)}
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {
+    "bf16": ["decode_bf16.cu", "decode_common.cuh", "decode_plan.cu", "pkv_device.cuh"],
+    "int4": ["int4.cu", "decode_common.cuh", "decode_plan.cu", "pkv_device.cuh"],
+}
+
+
+def source_hash(family: str = "bf16") -> str:
+    """Hash of the sources the attention kernels of one family are built from."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "paged_kv_cache_175_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[family]:
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -207,7 +214,8 @@ def recorded_traffic(workload: str):
         rec = json.load(open(p))[workload]
     except (OSError, KeyError, ValueError):
         return None
-    return rec["bytes_per_launch"] if rec.get("source_hash") == source_hash() else None
+    fam = "int4" if workload.startswith("int4") else "bf16"
+    return rec["bytes_per_launch"] if rec.get("source_hash") == source_hash(fam) else None
 
 
 # ---------------------------------------------------------------------------------------------
