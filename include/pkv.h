@@ -110,6 +110,11 @@ size_t pkv_decode_workspace_bytes(int batch, int n_h, int n_kv, int head_dim, in
  * accumulate; p is carried as a bf16 high + low pair), softmax online in fp32.
  * The result depends only on the logical token order, never on which physical
  * blocks hold the tokens.
+ * Kernel choice: groups of 17-32 query heads at head_dim 128 run, when the environment
+ * variable PKV_ATTN_KERNEL is "tc" at the time of the call, on the fifth-generation tensor
+ * cores (tcgen05.mma, 128-token tiles, accumulators in tensor memory, one CTA per SM);
+ * otherwise, and for every other shape, on warp-level mma.sync kernels (several CTAs per
+ * SM), which measured faster on that shape.  Same arithmetic and bounds either way.
  */
 pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, int max_blocks,

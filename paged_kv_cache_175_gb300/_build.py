@@ -10,8 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
-SOURCES = ["decode_plan.cu", "decode_bf16.cu", "int4.cu", "append_rope.cu", "offload.cu", "cacheblend.cu", "probe.cu", "block_manager.cpp"]
-HEADERS = ["pkv_device.cuh", "decode_common.cuh", "nvtx_range.h"]
+SOURCES = ["decode_plan.cu", "decode_bf16.cu", "decode_tc.cu", "int4.cu", "append_rope.cu", "offload.cu", "cacheblend.cu", "probe.cu", "block_manager.cpp"]
+HEADERS = ["pkv_device.cuh", "decode_common.cuh", "nvtx_range.h", "umma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -18,6 +18,7 @@
 // finished inside the piece are normalised and stored; cut segments store (m, l, O)
 // partials for the reduce kernel.
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "decode_common.cuh"
@@ -165,6 +166,8 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
       int flags = 0;
       if (pj == 0 || cur.blk == 0) flags |= F_FIRST;
       if (end || lb == cur.nb - 1) flags |= F_LAST;
+      if (cur.blk == 0) flags |= F_SEGB;
+      if (lb == cur.nb - 1) flags |= F_SEGE;
       if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
       if (pair) flags |= F_PAIR;
       if (end) flags |= F_END;
@@ -238,6 +241,7 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
     const int4 mt = meta[slot];
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;   // first q head of the group
+    if (warp == 0 && lane == 0) record_pieces(a, (long long)s * a.n_kv + g, flags, p);
 
     if (flags & F_FIRST) {
 #pragma unroll
@@ -418,6 +422,7 @@ struct Bf16Variant {
   size_t smem;
   int warps;
   int P;        // persistent CTAs on this device
+  bool tc;      // the tensor-memory kernel (takes the query tensor map as well)
 };
 
 template <int D, int BS, int NH, int MT, bool PW, int TB>
@@ -431,18 +436,29 @@ static Bf16Variant make_variant() {
   v.smem = bf16_smem_bytes<D, BS, TB>(v.stages);
   v.warps = MT + (PW ? 1 : 0);
   v.P = 0;
+  v.tc = false;
   return v;
+}
+
+// The tensor-memory kernel (decode_tc.cu) for groups of 17-32 heads at head_dim 128 is taken
+// when the environment variable PKV_ATTN_KERNEL is "tc" at the time of the call; by default
+// those groups run the mma.sync kernel, measured faster on this shape.
+static bool want_tc(int D, int tiling) {
+  if (D != 128 || tiling != 2) return false;
+  const char* e = getenv("PKV_ATTN_KERNEL");
+  return e && e[0] == 't' && e[1] == 'c' && e[2] == 0;
 }
 
 static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   // One table per process; the library drives one device per process.
   static std::mutex mu;
-  static Bf16Variant table[2][3][4];
-  static bool ready[2][3][4] = {};
+  static Bf16Variant table[2][3][4][2];
+  static bool ready[2][3][4][2] = {};
   const int di = D == 128 ? 1 : 0, bi = BS == 16 ? 0 : (BS == 32 ? 1 : 2), ti = tiling;
+  const int tc = want_tc(D, tiling) ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
-  Bf16Variant& v = table[di][bi][ti];
-  if (!ready[di][bi][ti]) {
+  Bf16Variant& v = table[di][bi][ti][tc];
+  if (!ready[di][bi][ti][tc]) {
 #define PKV_V(d, b)                                               \
   if (D == d && BS == b) {                                        \
     if (ti == 0) v = make_variant<d, b, 1, 1, true, 1>();         \
@@ -452,13 +468,27 @@ static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
   }
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
+    // groups of 17-32 heads at head_dim 128 on request: the kernel on the fifth-generation
+    // tensor cores (tiles of 128 tokens, accumulators in tensor memory); one CTA of 8 warps per SM
+    if (tc) {
+      const void* fn = nullptr;
+      size_t smem = 0;
+      if (tc_variant(BS, &fn, &smem)) {
+        v.fn = fn;
+        v.smem = smem;
+        v.warps = 8;
+        v.stages = 2;
+        v.stage_bytes = 0;
+        v.tc = true;
+      }
+    }
     if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v.smem) != cudaSuccess)
       return nullptr;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.warps * 32, v.smem) != cudaSuccess || occ < 1)
       return nullptr;
     v.P = device_sm_count() * occ;
-    ready[di][bi][ti] = true;
+    ready[di][bi][ti][tc] = true;
   }
   return &v;
 }
@@ -531,6 +561,7 @@ static pkv_status decode_bf16(const void* q, const void* k_pool, const void* v_p
   a.block_size = block_size;
   a.inline_plan = batch <= kInlinePlanSeqs;
   a.pieces = reinterpret_cast<int4*>(ws + wl.pieces);
+  a.seg_pp = reinterpret_cast<int2*>(ws + wl.segpp);
   a.batch = batch;
   a.n_h = n_h;
   a.n_kv = n_kv;
@@ -549,8 +580,17 @@ static pkv_status decode_bf16(const void* q, const void* k_pool, const void* v_p
   cudaError_t e = a.inline_plan ? cudaSuccess
                                 : launch_plan(context_lens, batch, max_blocks * block_size, block_size, a, v->P, st);
   if (e == cudaSuccess) {
-    void* kargs[] = {&tmk, &tmv, &a};
-    e = launch_pdl(v->fn, dim3(v->P), dim3(v->warps * 32), v->smem, st, kargs);
+    if (v->tc) {
+      // the group's 32 query rows of a segment, two 64-channel boxes
+      CUtensorMap tmq;
+      const uint64_t qrows = (uint64_t)batch * n_h;
+      if (encode_tensor_map_3d(&tmq, q, 128, qrows, 1, 256, 256 * qrows, 64, 32)) return PKV_ECUDA;
+      void* kargs[] = {&tmk, &tmv, &tmq, &a};
+      e = launch_pdl(v->fn, dim3(v->P), dim3(v->warps * 32), v->smem, st, kargs);
+    } else {
+      void* kargs[] = {&tmk, &tmv, &a};
+      e = launch_pdl(v->fn, dim3(v->P), dim3(v->warps * 32), v->smem, st, kargs);
+    }
   }
   if (e == cudaSuccess) e = launch_reduce(head_dim, a, v->P, st);
   if (e != cudaSuccess) {

@@ -166,85 +166,57 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int
 
 // ---- reduce: merge the partial softmax states of segments split across pieces ----------------
 // One warp per (sequence, q head).  Segments that fit in one piece were finished by the
-// attention kernel itself; empty sequences get a zero row here.
+// attention kernel itself; empty sequences get a zero row here.  The context length is
+// read before the grid-dependency wait (an input of the call, or the plan kernel's, which
+// finished before the attention kernel let this one launch), so that work overlaps the
+// attention kernel's tail; the pieces a segment spans come from the attention kernel.
 template <int D>
-__global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) {
-  // The plan kernel finished before the attention kernel started, so cum is readable
-  // before the grid-dependency wait: the index work overlaps the attention kernel's tail.
+__global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a) {
   constexpr int V = D / 32;                                   // channels per lane
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const bool live = row < a.batch * a.n_h;
-  int s = 0, h = 0, g = 0, hl = 0, nb = 0, p0 = 0, p1 = 0;
-  long long W = 0, seg = 0;
+  int nb = 0;
+  long long seg = 0;
   if (live) {
-    s = row / a.n_h; h = row % a.n_h; g = h / a.G; hl = h % a.G;
-    long long c0 = 0, total = 0;
-    if (a.inline_plan) {
-      // blocks of the sequences before s, of s, and of all, from the raw context lengths
-      constexpr int MAXC = kInlinePlanSeqs / 32;
-      const int nch = (a.batch + 31) / 32;
-      int cv[MAXC];
-#pragma unroll
-      for (int c = 0; c < MAXC; ++c) {
-        const int sq = c * 32 + lane;
-        cv[c] = (c < nch && sq < a.batch) ? a.ctx_raw[sq] : 0;
-      }
-#pragma unroll
-      for (int c = 0; c < MAXC; ++c) {
-        if (c >= nch) continue;
-        const int sq = c * 32 + lane;
-        const int b = span_blocks(clamp_ctx(cv[c], a.max_ctx), a.window, a.block_size);
-        int mine = sq == s ? b : 0, prev = sq < s ? b : 0, all = b;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          mine += __shfl_xor_sync(FULL_MASK, mine, o);
-          prev += __shfl_xor_sync(FULL_MASK, prev, o);
-          all += __shfl_xor_sync(FULL_MASK, all, o);
-        }
-        nb += mine;
-        c0 += prev;
-        total += all;
-      }
-    } else {
-      c0 = a.cum[s];
-      nb = a.cum[s + 1] - a.cum[s];
-      total = a.cum[a.batch];
-    }
-    W = (long long)a.n_kv * total;
-    P = effective_pieces(W, P);
-    if (nb > 0) {
-      const long long seg_start = (long long)a.n_kv * c0 + (long long)g * nb;
-      p0 = piece_of(seg_start, W, P);
-      p1 = piece_of(seg_start + nb - 1, W, P);
-    }
-    seg = (long long)s * a.n_kv + g;
+    const int s = row / a.n_h, h = row % a.n_h;
+    const int ctx = a.inline_plan ? clamp_ctx(a.ctx_raw[s], a.max_ctx) : a.ctx_eff[s];
+    nb = span_blocks(ctx, a.window, a.block_size);
+    seg = (long long)s * a.n_kv + h / a.G;
   }
   grid_dep_wait();
-  if (!live || (nb > 0 && p0 == p1)) return;                 // finished by the attention kernel
+  if (!live) return;
+  const int hl = (row % a.n_h) % a.G;
+  int p0 = 0, p1 = 0;
+  if (nb > 0) {
+    // the first and last pieces of the segment, recorded by the attention kernel
+    const int2 pp = a.seg_pp[seg];
+    if (pp.x == pp.y) return;                                 // finished by the attention kernel
+    p0 = pp.x;
+    p1 = pp.y;
+  }
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
   if (nb > 0) {
-    // Only pieces that hold part of the segment wrote a state.  When W < P some pieces
-    // are empty; the piece after p that holds data starts at line position b_{p+1}.
-    // Parts are merged in chunks of CH with every load of a chunk issued before any is
-    // used (one memory round trip per chunk instead of one per part), online across chunks.
+    // Every piece from p0 to p1 holds part of the segment (pieces hold at least 8 positions,
+    // so none is empty) and wrote a state.  Parts are merged in chunks of CH with every load
+    // of a chunk issued before any is used (one memory round trip per chunk instead of one
+    // per part), online across chunks.
     constexpr int CH = 8;
     float M = -INFINITY, L = 0.f;
-    int p = p0;
-    bool more = true;
-    while (more) {
+    for (int pc = p0; pc <= p1; pc += CH) {
       float mv[CH], lv[CH], ov[CH][V];
       bool use[CH];
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
-        use[i] = more;
+        const int p = pc + i;
+        use[i] = p <= p1;
         mv[i] = -INFINITY;
         lv[i] = 0.f;
 #pragma unroll
         for (int k = 0; k < V; ++k) ov[i][k] = 0.f;
-        if (more) {
+        if (use[i]) {
           const long long part = (seg + p) * a.G + hl;
           const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + part * 2);
           mv[i] = ml.x;
@@ -257,8 +229,6 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a, int P) 
             const float2 v = *reinterpret_cast<const float2*>(src);
             ov[i][0] = v.x; ov[i][1] = v.y;
           }
-          if (p == p1) more = false;
-          else p = piece_of(W * (p + 1) / P, W, P);
         }
       }
       float Mc = M;
@@ -299,7 +269,8 @@ cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t
   if (rows == 0) return cudaSuccess;
   dim3 grid((rows + 3) / 4), block(128);
   DecodeArgs args = a;
-  void* kargs[] = {&args, &P};
+  (void)P;
+  void* kargs[] = {&args};
   const void* fn = head_dim == 128 ? (const void*)reduce_kernel<128> : (const void*)reduce_kernel<64>;
   return launch_pdl(fn, grid, block, 0, stream, kargs);
 }
