@@ -33,60 +33,106 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
   }
 }
 
-// One CTA per listed block.  Angles delta * inv_freq[j] are formed in fp64, reduced
-// to [-pi, pi] in fp64 (k = rint(angle / 2pi)), and only the reduced angle goes to
-// the fp32 sincos, so large position deltas keep full fp32 accuracy.  The rotation
-// itself runs in fp32 on bf16 pairs and stores with round-to-nearest-even.
+// A CTA takes BPC consecutive listed blocks (so a CTA moves at least ~32 KB even when one
+// block is a few KB).  Angles delta * inv_freq[j] are formed in fp64 and reduced to
+// [-pi, pi] in fp64 (k = rint(angle / 2pi), taken as a product with 1 / 2pi), and only the
+// reduced angle goes to the fp32 sincos, so large position deltas keep full fp32 accuracy.
+// A block whose delta equals its predecessor's in the CTA reuses its table (the blocks of a
+// reused chunk share one delta).  The rotation runs in fp32 on bf16 pairs and stores with
+// round-to-nearest-even.
 struct RopeFreq {
   double inv_freq[64];
 };
+constexpr int kRopeMaxBPC = 8;
 
 template <int D>
 __global__ void __launch_bounds__(256) rope_shift_kernel(__nv_bfloat16* __restrict__ k_pool,
                                                          const int32_t* __restrict__ block_ids,
-                                                         const int32_t* __restrict__ deltas, int num_blocks,
-                                                         int n_kv, int block_size, const RopeFreq f, int32_t* err) {
+                                                         const int32_t* __restrict__ deltas, int n_blocks,
+                                                         int num_blocks, int n_kv, int block_size, int bpc,
+                                                         const RopeFreq f, int32_t* err) {
   constexpr int H = D / 2;
-  __shared__ float cs[H], sn[H];
-  const int phys = block_ids[blockIdx.x];
-  const int delta = deltas[blockIdx.x];
-  if ((unsigned)phys >= (unsigned)num_blocks) {
-    if (threadIdx.x == 0) set_err(err, PKV_DEV_BAD_BLOCK);
-    return;
-  }
-  if (delta == 0) return;                                     // rotation by 0 is the identity
-  const double two_pi = 6.283185307179586476925286766559;
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const double ang = (double)delta * f.inv_freq[j];
-    const double r = ang - rint(ang / two_pi) * two_pi;
-    float sv, cv;
-    sincosf((float)r, &sv, &cv);
-    cs[j] = cv;
-    sn[j] = sv;
+  __shared__ float cs[kRopeMaxBPC][H], sn[kRopeMaxBPC][H];
+  __shared__ int tab[kRopeMaxBPC];                           // table of each block slot
+  __shared__ int phys_s[kRopeMaxBPC], delta_s[kRopeMaxBPC];
+  const int b0 = blockIdx.x * bpc;
+  const int nb = n_blocks - b0 < bpc ? n_blocks - b0 : bpc;
+  if (threadIdx.x < nb) {
+    const int ph = block_ids[b0 + threadIdx.x], dl = deltas[b0 + threadIdx.x];
+    const bool okb = (unsigned)ph < (unsigned)num_blocks;
+    if (!okb) set_err(err, PKV_DEV_BAD_BLOCK);
+    phys_s[threadIdx.x] = okb ? ph : -1;
+    delta_s[threadIdx.x] = dl;
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < nb; ++b) tab[b] = (b > 0 && delta_s[b] == delta_s[b - 1]) ? tab[b - 1] : b;
+  }
   const int rows = n_kv * block_size;
   // one 16-byte vector of each half of a row per item: channels j0..j0+7 and their partners
   constexpr int V = H / 8;                                    // vectors per half row
-  uint4* base = reinterpret_cast<uint4*>(k_pool + (size_t)phys * rows * D);
-  for (int idx = threadIdx.x; idx < rows * V; idx += blockDim.x) {
-    const int r = idx / V, v = idx - r * V;
-    uint4* row = base + (size_t)r * (D / 8);
-    uint4 a = row[v], b = row[v + V];
-    const int j0 = 8 * v;
-    auto rot = [&](uint32_t& wa, uint32_t& wb, int j) {     // channels j, j + 1 and j + H, j + H + 1
-      const float x1a = bf16_lo(wa), x1b = bf16_hi(wa), x2a = bf16_lo(wb), x2b = bf16_hi(wb);
-      const float y1a = x1a * cs[j] - x2a * sn[j], y1b = x1b * cs[j + 1] - x2b * sn[j + 1];
-      const float y2a = x1a * sn[j] + x2a * cs[j], y2b = x1b * sn[j + 1] + x2b * cs[j + 1];
-      wa = pack_bf16(y1a, y1b);
-      wb = pack_bf16(y2a, y2b);
-    };
-    rot(a.x, b.x, j0);
-    rot(a.y, b.y, j0 + 2);
-    rot(a.z, b.z, j0 + 4);
-    rot(a.w, b.w, j0 + 6);
-    row[v] = a;
-    row[v + V] = b;
+  constexpr int NI = 4;                                       // items in flight per thread
+  const int per_block = rows * V, total = nb * per_block;
+  // the first items' keys are loaded before the angle tables are built, so the loads and the
+  // fp64 / sincos work overlap
+  uint4 av[NI], bv[NI];
+  uint4* rp[NI];
+  auto load = [&](int base) {
+#pragma unroll
+    for (int k = 0; k < NI; ++k) {
+      const int idx = base + k * blockDim.x;
+      rp[k] = nullptr;
+      if (idx < total) {
+        const int b = idx / per_block, rem = idx - b * per_block;
+        const int phys = phys_s[b];
+        if (phys >= 0 && delta_s[b] != 0) {                  // else a bad id (flagged) or the identity
+          const int r = rem / V;
+          rp[k] = reinterpret_cast<uint4*>(k_pool + ((size_t)phys * rows + r) * D) + (rem - r * V);
+          av[k] = rp[k][0];
+          bv[k] = rp[k][V];
+        }
+      }
+    }
+  };
+  load(threadIdx.x);
+  __syncthreads();                                            // tab
+  const double two_pi = 6.283185307179586476925286766559, inv_two_pi = 0.15915494309189533576888376337251;
+  for (int e = threadIdx.x; e < nb * H; e += blockDim.x) {
+    const int b = e / H, j = e - b * H;
+    if (tab[b] != b || delta_s[b] == 0) continue;
+    const double ang = (double)delta_s[b] * f.inv_freq[j];
+    const double r = fma(-rint(ang * inv_two_pi), two_pi, ang);
+    float sv, cv;
+    sincosf((float)r, &sv, &cv);
+    cs[b][j] = cv;
+    sn[b][j] = sv;
+  }
+  __syncthreads();
+  for (int base = threadIdx.x;; base += NI * blockDim.x) {
+#pragma unroll
+    for (int k = 0; k < NI; ++k) {
+      if (!rp[k]) continue;
+      const int idx = base + k * blockDim.x;
+      const int b = idx / per_block, rem = idx - b * per_block;
+      const float* c = cs[tab[b]];
+      const float* sr = sn[tab[b]];
+      const int j0 = 8 * (rem % V);
+      auto rot = [&](uint32_t& wa, uint32_t& wb, int j) {   // channels j, j + 1 and j + H, j + H + 1
+        const float x1a = bf16_lo(wa), x1b = bf16_hi(wa), x2a = bf16_lo(wb), x2b = bf16_hi(wb);
+        const float y1a = x1a * c[j] - x2a * sr[j], y1b = x1b * c[j + 1] - x2b * sr[j + 1];
+        const float y2a = x1a * sr[j] + x2a * c[j], y2b = x1b * sr[j + 1] + x2b * c[j + 1];
+        wa = pack_bf16(y1a, y1b);
+        wb = pack_bf16(y2a, y2b);
+      };
+      rot(av[k].x, bv[k].x, j0);
+      rot(av[k].y, bv[k].y, j0 + 2);
+      rot(av[k].z, bv[k].z, j0 + 4);
+      rot(av[k].w, bv[k].w, j0 + 6);
+      rp[k][0] = av[k];
+      rp[k][V] = bv[k];
+    }
+    if (base + NI * blockDim.x >= total) break;
+    load(base + NI * blockDim.x);
   }
 }
 
@@ -136,15 +182,20 @@ extern "C" pkv_status pkv_rope_shift_k(void* k_pool, const int32_t* block_ids, c
   RopeFreq f = {};
   for (int j = 0; j < head_dim / 2; ++j) f.inv_freq[j] = std::pow(rope_base, -2.0 * j / head_dim);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // one thread per 16-byte vector pair of a block, at most 256 (they loop), at least 64
-  const long long items = (long long)n_kv * block_size * (head_dim / 16);
+  // consecutive listed blocks per CTA: about 32 KB of keys per CTA, at most kRopeMaxBPC
+  const long long block_bytes = (long long)n_kv * block_size * head_dim * 2;
+  int bpc = (int)((32768 + block_bytes - 1) / block_bytes);
+  bpc = bpc < 1 ? 1 : (bpc > kRopeMaxBPC ? kRopeMaxBPC : bpc);
+  // one thread per 16-byte vector pair, at most 256 (they loop), at least 64
+  const long long items = (long long)bpc * n_kv * block_size * (head_dim / 16);
   const int threads = items >= 256 ? 256 : (items <= 64 ? 64 : (int)((items + 31) / 32 * 32));
+  const unsigned grid = (unsigned)((n_blocks + bpc - 1) / bpc);
   if (head_dim == 128)
-    rope_shift_kernel<128><<<n_blocks, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
-                                                         num_blocks, n_kv, block_size, f, err_flag);
+    rope_shift_kernel<128><<<grid, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
+                                                     n_blocks, num_blocks, n_kv, block_size, bpc, f, err_flag);
   else
-    rope_shift_kernel<64><<<n_blocks, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
-                                                        num_blocks, n_kv, block_size, f, err_flag);
+    rope_shift_kernel<64><<<grid, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
+                                                    n_blocks, num_blocks, n_kv, block_size, bpc, f, err_flag);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);

@@ -22,6 +22,85 @@ __host__ __device__ inline int dev_lanes_per_token(int vec_per_tok) {
   return l;
 }
 
+// Rows of at most `lpt` vectors (one vector per lane and tensor: n_kv * head_dim <= 256,
+// the MQA shapes): each lane group takes kDevTok tokens per pass, with every slot load, then
+// every data load of the pass issued before any is used -- four times the bytes in flight
+// of one token per pass, which a short row leaves too few of to cover the memory latency.
+constexpr int kDevTok = 4;
+
+__global__ void __launch_bounds__(kDevThreads)
+    kv_deviation_short_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
+                              const int64_t* __restrict__ slots, const uint4* __restrict__ k_new,
+                              const uint4* __restrict__ v_new, long long n, int n_kv, int block_size,
+                              int vec_per_row, long long n_slots, int bs_shift, int vpr_shift, float* __restrict__ dev,
+                              int32_t* err) {
+  grid_dep_launch();                       // a following selection may launch; it waits for this grid
+  const int lane = threadIdx.x & 31;
+  const int vec_per_tok = n_kv * vec_per_row;
+  const int lpt = dev_lanes_per_token(vec_per_tok), tpw = 32 / lpt;
+  const int sub = lane / lpt, sl = lane % lpt;
+  const long long groups = (long long)gridDim.x * (kDevThreads / 32) * tpw;
+  const long long gq = (blockIdx.x * (long long)(kDevThreads / 32) + (threadIdx.x >> 5)) * tpw + sub;
+  const bool has_vec = sl < vec_per_tok;
+  int g = 0, w = sl;
+  if (has_vec) {
+    g = vpr_shift >= 0 ? sl >> vpr_shift : sl / vec_per_row;
+    w = sl - g * vec_per_row;
+  }
+  for (long long base = 0; base < n; base += kDevTok * groups) {   // the same passes in every lane
+    long long slot[kDevTok];
+    bool live[kDevTok], bad[kDevTok];
+    uint4 a[kDevTok], b[kDevTok], c[kDevTok], d[kDevTok];
+#pragma unroll
+    for (int u = 0; u < kDevTok; ++u) {                 // slots and recomputed rows (independent)
+      const long long t = base + u * groups + gq;
+      slot[u] = t < n ? slots[t] : 0;
+      if (t < n && has_vec) {
+        c[u] = __ldg(k_new + t * vec_per_tok + sl);
+        d[u] = __ldg(v_new + t * vec_per_tok + sl);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kDevTok; ++u) {                 // then the cached rows the slots point at
+      const long long t = base + u * groups + gq;
+      bad[u] = t < n && (slot[u] < 0 || slot[u] >= n_slots);
+      live[u] = t < n && !bad[u];
+      if (live[u] && has_vec) {
+        const long long blk = bs_shift >= 0 ? slot[u] >> bs_shift : slot[u] / block_size;
+        const long long row = slot[u] - blk * block_size;
+        const size_t src = (((size_t)blk * n_kv + g) * block_size + row) * vec_per_row + w;
+        a[u] = __ldg(k_pool + src);
+        b[u] = __ldg(v_pool + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kDevTok; ++u) {
+      float acc = 0.f;
+      if (live[u] && has_vec) {
+        const uint32_t* pa = reinterpret_cast<const uint32_t*>(&a[u]);
+        const uint32_t* pb = reinterpret_cast<const uint32_t*>(&b[u]);
+        const uint32_t* pc = reinterpret_cast<const uint32_t*>(&c[u]);
+        const uint32_t* pd = reinterpret_cast<const uint32_t*>(&d[u]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float k0 = bf16_lo(pa[j]) - bf16_lo(pc[j]), k1 = bf16_hi(pa[j]) - bf16_hi(pc[j]);
+          const float v0 = bf16_lo(pb[j]) - bf16_lo(pd[j]), v1 = bf16_hi(pb[j]) - bf16_hi(pd[j]);
+          acc = fmaf(k0, k0, acc);
+          acc = fmaf(k1, k1, acc);
+          acc = fmaf(v0, v0, acc);
+          acc = fmaf(v1, v1, acc);
+        }
+      }
+      for (int o = lpt / 2; o; o >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, o);   // within the group
+      const long long t = base + u * groups + gq;
+      if (sl == 0 && t < n) {
+        if (bad[u]) set_err(err, PKV_DEV_BAD_SLOT);
+        dev[t] = bad[u] ? 0.f : sqrtf(acc);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kDevThreads)
     kv_deviation_kernel(const uint4* __restrict__ k_pool, const uint4* __restrict__ v_pool,
                         const int64_t* __restrict__ slots, const uint4* __restrict__ k_new,
@@ -280,6 +359,23 @@ extern "C" pkv_status pkv_kv_deviation(const void* k_pool, const void* v_pool, c
   if (!al16(k_pool) || !al16(v_pool) || !al16(k_new) || !al16(v_new)) return PKV_EINVAL;
   const int vpr = head_dim / 8;
   const int tokens_per_cta = kDevThreads / 32 * (32 / dev_lanes_per_token(n_kv * vpr));
+  if (n_kv * vpr <= dev_lanes_per_token(n_kv * vpr)) {
+    // one vector per lane and tensor: kDevTok tokens per lane group and pass
+    // a persistent grid of the CTAs that fit at once (two per SM at this kernel's registers);
+    // the lanes loop over passes
+    const long long want = ((long long)n + tokens_per_cta * kDevTok - 1) / (tokens_per_cta * kDevTok);
+    const int grid = (int)(want < 2LL * device_sm_count() ? want : 2LL * device_sm_count());
+    kv_deviation_short_kernel<<<grid, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), slots,
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), n, n_kv, block_size, vpr,
+        (long long)num_blocks * block_size, log2_if_pow2(block_size), log2_if_pow2(vpr), dev, err_flag);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      record_cuda_error(e);
+      return PKV_ECUDA;
+    }
+    return PKV_OK;
+  }
   const long long want = ((long long)n + tokens_per_cta - 1) / tokens_per_cta;
   const int grid = (int)(want < 16LL * device_sm_count() ? want : 16LL * device_sm_count());
   kv_deviation_kernel<<<grid, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(
