@@ -469,14 +469,14 @@ static Bf16Variant* lookup_bf16(int D, int BS, int tiling) {
     PKV_V(64, 16) PKV_V(64, 32) PKV_V(64, 64) PKV_V(128, 16) PKV_V(128, 32) PKV_V(128, 64)
 #undef PKV_V
     // groups of 17-32 heads at head_dim 128 on request: the kernel on the fifth-generation
-    // tensor cores (tiles of 128 tokens, accumulators in tensor memory); one CTA of 8 warps per SM
+    // tensor cores (tiles of 128 tokens, accumulators in tensor memory); one CTA of 12 warps per SM
     if (tc) {
       const void* fn = nullptr;
       size_t smem = 0;
       if (tc_variant(BS, &fn, &smem)) {
         v.fn = fn;
         v.smem = smem;
-        v.warps = 8;
+        v.warps = 12;
         v.stages = 2;
         v.stage_bytes = 0;
         v.tc = true;

@@ -3,25 +3,28 @@
 //
 // Same work partition as the other attention kernels (decode_common.cuh): a persistent CTA
 // per SM streams piece p of the (sequence, kv head, block) line.  A tile is up to 128
-// tokens -- consecutive blocks of one segment -- and each CTA runs three roles:
-//   warps 0, 7   producers: each walks the piece and per tile issues the TMA loads of its K
-//                (warp 0) or V (warp 7) blocks (128-byte swizzle, 64-channel boxes) into a
+// tokens -- consecutive blocks of one segment -- and each CTA of 12 warps runs four roles:
+//   warps 0, 3   producers: each walks the piece and per tile issues the TMA loads of its K
+//                (warp 0) or V (warp 3) blocks (128-byte swizzle, 64-channel boxes) into a
 //                ring of 32 KB stages -- 2 for K, freed by the first product, 4 for V, freed
 //                by the second -- and warp 0 per segment the group's 32 query rows;
 //   warp 1       owner of the tensor memory; one thread issues the first product
 //                  S^T[tokens][heads] = K Q^T   (M 128, N 32, K 128; both K-major)
 //                into one of two S buffers as soon as a tile's stage has landed;
-//   warps 2-5    softmax and epilogue: thread r owns token row r of S^T and channel row r
-//                of O^T;
-//   warp 6       one thread issues the second product once the group has written P
+//   warps 4-11   softmax and epilogue, in two groups of four warps: group g takes heads
+//                [16 g, 16 g + 16), and its thread r owns token row r of S^T and channel row
+//                r of O^T for those heads (each SM sub-partition runs one role warp and one
+//                warp of each group, so the two groups' tiles overlap);
+//   warp 2       one thread issues the second product once both groups have written P
 //                  O^T[ch][2 x heads] += V^T [P_hi | P_lo]^T
 //                                              (M 128, N 64, K = the tile's tokens; V and
 //                                               P MN-major, as they lie in shared memory)
-//                into one of two O buffers (segment parity).  Online softmax in base 2 with the scale folded in and a lazy
-//                offset (raised only when a score exceeds it by more than 8; the raise
-//                rescales l and the O columns in tensor memory).  P is written to shared
-//                memory as a bf16 high part and a bf16 low part (columns 0-31 / 32-63 of
-//                the second product's B operand), so P's rounding is below 2^-16.
+//                into one of two O buffers (segment parity).
+// Online softmax in base 2 with the scale folded in and a lazy offset (raised only when a
+// score exceeds it by more than 8; the raise rescales the O columns in tensor memory and
+// each thread's share of the sums l, which the group adds up at the segment's end).  P is
+// written to shared memory as a bf16 high part and a bf16 low part (columns 0-31 / 32-63 of
+// the second product's B operand), so P's rounding is below 2^-16.
 // Rows outside [lead, ntok) and rows of blocks with a bad id get p = 0; their V rows are
 // zeroed before the product reads them (a stale row may hold NaN or inf).
 #include <cmath>
@@ -54,13 +57,11 @@ struct TcLayout {
   static constexpr int META = (NK + NV) * (int)sizeof(TcTileMeta);
   static constexpr int NBAR = 28;
   static constexpr int RED_OFF = M_OFF + META + NBAR * 8 + 8;
-  // 8 rows x 16 bytes of bf16 ones; a descriptor start address is a multiple of 16 bytes
-  static constexpr int ONES_OFF = (RED_OFF + 4 * 32 * 4 + 127) / 128 * 128;
-  static constexpr int BYTES = ONES_OFF + 128;
+  static constexpr int BYTES = RED_OFF + 256 * 4;
   static constexpr size_t SMEM = 1024 + (size_t)BYTES;  // with the 1024-byte alignment slack
-  static_assert(ONES_OFF % 128 == 0 && Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "descriptor alignment");
+  static_assert(Q_OFF % 1024 == 0 && P_OFF % 1024 == 0, "descriptor alignment");
   static_assert(SMEM <= 232448, "shared memory of one CTA");
-  static constexpr uint32_t TMEM_COLS = 512;          // S[2] at 0 / 32, O[2] at 64 / 128, l[2] at 192 / 256
+  static constexpr uint32_t TMEM_COLS = 256;          // S[2] at 0 / 32, O[2] at 64 / 128
 };
 
 // mbarriers: the K ring (full / empty, 2 each), the V ring (4 each), query buffers, S buffers
@@ -77,7 +78,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 
 template <int BS>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmq, const DecodeArgs a) {
   using L = TcLayout<BS>;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(256, 1)
   TcTileMeta* vmeta = kmeta + L::NK;                                    // per V stage
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::M_OFF + L::META);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + L::NBAR);
-  float* red = reinterpret_cast<float*>(sm + L::RED_OFF);          // [4][32] reduction scratch
+  float* red = reinterpret_cast<float*>(sm + L::RED_OFF);          // 256 floats of reduction scratch
   __shared__ volatile int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -96,15 +97,13 @@ __global__ void __launch_bounds__(256, 1)
     abort_flag = 0;
     for (int b = 0; b < L::NBAR; ++b)
       mbar_init(&bar[b], (b == BAR_SEMPTY || b == BAR_SEMPTY + 1 || b == BAR_PFULL || b == BAR_OEMPTY ||
-                          b == BAR_OEMPTY + 1) ? 4 : 1);
+                          b == BAR_OEMPTY + 1) ? 8 : 1);     // one arrival per softmax warp
     fence_barrier_init();
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
     prefetch_tensormap(&tmq);
   }
   if (warp == 1) tmem_alloc(tmem_slot, L::TMEM_COLS);
-  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(sm + L::ONES_OFF)[threadIdx.x] = 0x3f803f80u;   // bf16 1, 1
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -114,7 +113,7 @@ __global__ void __launch_bounds__(256, 1)
 
   Cursor cur;
   PieceInfo pi;
-  piece_setup(a, blockIdx.x, gridDim.x, warp == 0 || warp == 7, cur, pi);   // both producers walk the piece
+  piece_setup(a, blockIdx.x, gridDim.x, warp == 0 || warp == 3, cur, pi);   // both producers walk the piece
   const int P = pi.P, p = blockIdx.x;
   const long long pstart = pi.pstart, pend = pi.pend;
   const int len = p < P ? (int)(pend - pstart) : 0;
@@ -124,10 +123,10 @@ __global__ void __launch_bounds__(256, 1)
   if (a.inline_plan) grid_dep_wait();
 
   if (len > 0) {
-    if (warp == 0 || warp == 7) {
+    if (warp == 0 || warp == 3) {
       // ------------------------------- producers -------------------------------
       // Warp 0 loads K (and, per segment, the group's queries) into a ring of NK stages;
-      // warp 7 loads V into a ring of NV stages.  Each walks the same tiles and keeps one tile
+      // warp 3 loads V into a ring of NV stages.  Each walks the same tiles and keeps one tile
       // ahead: the next tile's block ids are fetched while it waits for a free stage, and a
       // tile's copies (2 per block: two 64-channel boxes) go out from one lane each.  K is
       // free again once the first product has run, V only after the second, so the V ring is
@@ -276,13 +275,12 @@ __global__ void __launch_bounds__(256, 1)
         mbar_wait(&bar[BAR_DRAIN], 0);
       }
       __syncwarp();                     // the warp reaches the CTA barrier converged
-    } else if (warp == 6) {
+    } else if (warp == 2) {
       // ------------------------- second-product issuer ------------------------
-      // O^T[segment parity] += V^T [P_hi | P_lo]^T once the softmax group has written tile
+      // O^T[segment parity] += V^T [P_hi | P_lo]^T once the softmax groups have written tile
       // i's P (and, for a segment's first tile, has read the O buffer's previous segment).
       if (lane == 0) {
         constexpr uint32_t IPV = umma_idesc_bf16(128, 64, 1, 1);
-        constexpr uint32_t IPV_ONES = umma_idesc_bf16(128, 64, 0, 1);   // A K-major (no swizzle)
         const uint32_t sbase = smem_u32(sm);
         bool ok = true;
         for (int i = 0;; ++i) {
@@ -301,16 +299,11 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t vb = sbase + L::V_OFF + slot * L::KVST, pb = sbase + L::P_OFF;
           const uint32_t od = tmem + 64 + 64 * ob;
           const int nks = (ntok + 15) >> 4;
-          // the softmax sums: an all-ones A (every row, every k the same 16 bytes of ones, so
-          // both offsets are 0) against the same P gives sum_t p_t of every head column in
-          // every row of l[segment parity]
-          const uint64_t ones = umma_desc(sbase + L::ONES_OFF, 0, 0, 0);
           for (int kk = 0; kk < nks; ++kk) {
             const uint64_t ad = umma_desc(vb + kk * 2048, L::CHUNK, 1024, kLayoutSw128);
             const uint64_t bd = umma_desc(pb + kk * 2048, L::CHUNK, 1024, kLayoutSw128);
             const uint32_t acc = ((flags & F_FIRST) && kk == 0) ? 0u : 1u;
             umma_bf16(od, ad, bd, IPV, acc);
-            umma_bf16(tmem + 192 + 64 * ob, ones, bd, IPV_ONES, acc);
           }
           umma_commit(&bar[BAR_VEMPTY + slot]);
           umma_commit(&bar[BAR_PEMPTY]);
@@ -327,12 +320,19 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
     } else {
       // -------------------------- softmax and epilogue ------------------------
-      const int wq = warp & 3;                       // this warp's quarter of the tensor-memory lanes
-      const int row = 32 * wq + lane;                // token row of S^T, channel row of O^T
+      // Group gi of four warps takes heads [hb, hb + 16); warp w reaches the tensor-memory
+      // lanes of quarter w % 4, so thread r of a group owns token row r of S^T and channel
+      // row r of O^T for its heads.
+      const int wq = warp & 3, gi = (warp - 4) >> 2, hb = 16 * gi;
+      const int row = 32 * wq + lane;
       const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
-      float m[32];                                   // running offsets, the same in every thread
-      // A failed (timed-out) wait makes `bad` true for the whole warp; the group learns of it at
-      // the vote that opens each tile and leaves together, so no thread is left at a named
+      float* redg = red + 64 * gi;                    // [4 warps][16 heads]: the group's maxima
+      float* red_m = red + 128;                       // the segment's offsets and sums, 32 heads
+      float* red_l = red + 160;
+      float m[16], l[16];                             // running offsets (the same in every thread) and
+                                                      // this thread's rows' share of the softmax sums
+      // A failed (timed-out) wait makes `bad` true for the whole warp; both groups learn of it
+      // at the vote that opens each tile and leave together, so no thread is left at a named
       // barrier.  Within a tile every named barrier is passed whatever happened.
       bool bad = false;
       int i = 0;
@@ -341,46 +341,50 @@ __global__ void __launch_bounds__(256, 1)
         bool okw = !bad && !abort_flag && mbar_wait(&bar[BAR_VFULL + slot], (i / L::NV) & 1) &&
                    mbar_wait(&bar[BAR_SFULL + sb], (i >> 1) & 1);
         okw = __all_sync(FULL_MASK, okw);
-        if (named_bar_or(1, 128, !okw)) {
+        if (named_bar_or(1, 256, !okw)) {
           bad = true;
           break;
         }
         const TcTileMeta mt = vmeta[slot];
         const int ntok = mt.rows & 255, flags = (mt.rows >> 8) & 255, lead = mt.rows >> 16, ob = mt.k & 1;
-        if (threadIdx.x == 64) record_pieces(a, (long long)mt.s * a.n_kv + mt.g, flags, p);
+        if (threadIdx.x == 128) record_pieces(a, (long long)mt.s * a.n_kv + mt.g, flags, p);
         tc_fence_after();
-        float x[32];
+        float x[16];
         {
-          uint32_t sr[32];
-          tmem_ld32(tmem + lane_off + 32 * sb, sr);
+          uint32_t sr[16];
+          tmem_ld16(tmem + lane_off + 32 * sb + hb, sr);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(sr[h]) * a.scale_log2;
+          for (int h = 0; h < 16; ++h) x[h] = __uint_as_float(sr[h]) * a.scale_log2;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[BAR_SEMPTY + sb]);     // S buffer sb may be rewritten
         if (flags & F_FIRST) {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) m[h] = -INFINITY;
+          for (int h = 0; h < 16; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+          }
         }
         const bool valid = row >= lead && row < ntok && !((mt.invalid >> (row / BS)) & 1);
         bool over = false;
         if (valid) {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) over |= x[h] > m[h] + kLazyMax;
+          for (int h = 0; h < 16; ++h) over |= x[h] > m[h] + kLazyMax;
         } else {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) x[h] = -INFINITY;
+          for (int h = 0; h < 16; ++h) x[h] = -INFINITY;
         }
-        if (named_bar_or(1, 128, over)) {
-          // raise the offsets to the running max.  A reduce-scatter over the warp leaves the
-          // warp's max of head `lane` in v[0]; the four warps' maxima meet in shared memory.
-          float v[32];
+        if (named_bar_or(2 + gi, 128, over)) {
+          // raise the group's offsets to the running max.  After the exchange across the two
+          // half-warps, a reduce-scatter leaves the warp's max of head hb + (lane & 15) in
+          // v[0]; the four warps' maxima meet in shared memory.
+          float v[16];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = x[h];
+          for (int h = 0; h < 16; ++h) v[h] = fmaxf(x[h], __shfl_xor_sync(FULL_MASK, x[h], 16));
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
+          for (int o = 8; o >= 1; o >>= 1) {
             const bool up = lane & o;
 #pragma unroll
             for (int j = 0; j < o; ++j) {
@@ -388,32 +392,34 @@ __global__ void __launch_bounds__(256, 1)
               v[j] = fmaxf(keep, __shfl_xor_sync(FULL_MASK, send, o));
             }
           }
-          red[wq * 32 + lane] = v[0];
-          named_bar(2, 128);
-          const float mx = fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
-          named_bar(2, 128);
-          float al[32];
+          if (lane < 16) redg[wq * 16 + lane] = v[0];
+          named_bar(4 + gi, 128);
+          const int hl = lane & 15;
+          const float mx = fmaxf(fmaxf(redg[hl], redg[16 + hl]), fmaxf(redg[32 + hl], redg[48 + hl]));
+          named_bar(4 + gi, 128);
+          float al[16];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
+          for (int h = 0; h < 16; ++h) {
             const float mn = fmaxf(m[h], __shfl_sync(FULL_MASK, mx, h));
             al[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
             m[h] = mn;
+            l[h] *= al[h];
           }
           if (!(flags & F_FIRST)) {
-            // O and the softmax sums accumulated so far: wait for the previous tile's products,
-            // then scale the high and low columns of each head in place
+            // O accumulated so far: wait for the previous tile's products, then scale the
+            // group's high and low columns in place
             bad |= !__all_sync(FULL_MASK, mbar_wait(&bar[BAR_PEMPTY], (i - 1) & 1));
             if (!bad) {
               tc_fence_after();
 #pragma unroll 1
-              for (int part = 0; part < 4; ++part) {
-                const uint32_t ta = tmem + lane_off + (part < 2 ? 64 + 64 * ob : 192 + 64 * ob) + 32 * (part & 1);
-                uint32_t orr[32];
-                tmem_ld32(ta, orr);
+              for (int part = 0; part < 2; ++part) {
+                const uint32_t ta = tmem + lane_off + 64 + 64 * ob + 32 * part + hb;
+                uint32_t orr[16];
+                tmem_ld16(ta, orr);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 32; ++h) orr[h] = __float_as_uint(__uint_as_float(orr[h]) * al[h]);
-                tmem_st32(ta, orr);
+                for (int h = 0; h < 16; ++h) orr[h] = __float_as_uint(__uint_as_float(orr[h]) * al[h]);
+                tmem_st16(ta, orr);
                 tmem_wait_st();
               }
               tc_fence_before();
@@ -422,34 +428,35 @@ __global__ void __launch_bounds__(256, 1)
         }
         // the P buffer is free once the products of tile i - 1 have completed
         if (i >= 1) bad |= !__all_sync(FULL_MASK, mbar_wait(&bar[BAR_PEMPTY], (i - 1) & 1));
-        uint32_t ph[16], pl[16];
+        uint32_t ph[8], pl[8];
 #pragma unroll
-        for (int h2 = 0; h2 < 16; ++h2) {
+        for (int h2 = 0; h2 < 8; ++h2) {
           float pv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int h = 2 * h2 + e;
             pv[e] = valid ? ex2(x[h] - m[h]) : 0.f;
+            l[h] += pv[e];
           }
           ph[h2] = pack_bf16(pv[0], pv[1]);
           pl[h2] = pack_bf16(pv[0] - bf16_lo(ph[h2]), pv[1] - bf16_hi(ph[h2]));
         }
         // row `row` of the B operand: 128 bytes (high parts of heads 0-31, then low parts),
-        // 16-byte chunk c stored at chunk c ^ (row % 8) (128-byte swizzle)
+        // 16-byte chunk c stored at chunk c ^ (row % 8) (128-byte swizzle); this group's
+        // heads are chunks 2 gi, 2 gi + 1 (high) and 4 + 2 gi, 5 + 2 gi (low)
         uint8_t* prow = sm + L::P_OFF + row * 128;
         if (!bad) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t* src = c < 4 ? ph + 4 * c : pl + 4 * (c - 4);
-            *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
+          for (int c = 0; c < 2; ++c) {
+            *reinterpret_cast<uint4*>(prow + (((2 * gi + c) ^ (row & 7)) << 4)) =
+                make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
+            *reinterpret_cast<uint4*>(prow + (((4 + 2 * gi + c) ^ (row & 7)) << 4)) =
+                make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
           }
           if (!valid && row < ((ntok + 15) & ~15)) {      // a V row the product reads with p = 0
-            uint8_t* vrow = sm + L::V_OFF + slot * L::KVST + row * 128;
+            uint8_t* vrow = sm + L::V_OFF + slot * L::KVST + gi * L::CHUNK + row * 128;   // this group's half
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(vrow + L::CHUNK + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         fence_proxy_async_smem();          // the rows written above, for the tensor core
@@ -457,70 +464,87 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0 && !bad) mbar_arrive(&bar[BAR_PFULL]);
 
         if (flags & F_LAST) {
-          // O^T and the softmax sums of the segment (every lane of the sums holds the same
-          // values), once its products have completed; then O / l through shared memory (the P
-          // buffer, which those products were the last to read) to coalesced stores
+          // The segment's softmax sums of the group's heads: a reduce-scatter over the warp
+          // leaves the warp's sum of head hb + (lane & 15) in v[0], and the four warps' sums
+          // meet in shared memory.  Then O^T of those heads, once the segment's products have
+          // completed, and O / l through shared memory (the P buffer, which those products were
+          // the last to read) to coalesced stores.
+          float ls[16];
+          {
+            float v[16];
+#pragma unroll
+            for (int h = 0; h < 16; ++h) v[h] = l[h] + __shfl_xor_sync(FULL_MASK, l[h], 16);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) {
+              const bool up = lane & o;
+#pragma unroll
+              for (int j = 0; j < o; ++j) {
+                const float keep = up ? v[j + o] : v[j], send = up ? v[j] : v[j + o];
+                v[j] = keep + __shfl_xor_sync(FULL_MASK, send, o);
+              }
+            }
+            if (lane < 16) redg[wq * 16 + lane] = v[0];
+            named_bar(4 + gi, 128);
+            const int hl = lane & 15;
+            const float tot = (redg[hl] + redg[16 + hl]) + (redg[32 + hl] + redg[48 + hl]);
+            named_bar(4 + gi, 128);
+#pragma unroll
+            for (int h = 0; h < 16; ++h) ls[h] = __shfl_sync(FULL_MASK, tot, h);
+          }
           bad |= !__all_sync(FULL_MASK, !bad && mbar_wait(&bar[BAR_OFULL + ob], (mt.k >> 1) & 1));
           const bool whole = flags & F_WHOLE;
           float* scr = reinterpret_cast<float*>(sm + L::P_OFF);          // [128 channels][32 heads]
           if (!bad) {
             tc_fence_after();
-#pragma unroll 1
-            for (int hb = 0; hb < 32; hb += 16) {                       // heads hb .. hb + 15
-              const uint32_t oc = tmem + lane_off + 64 + 64 * ob + hb, lc = tmem + lane_off + 192 + 64 * ob + hb;
-              uint32_t t0[16], t1[16];
-              float o[16], ls[16];
-              tmem_ld16(lc, t0);
-              tmem_ld16(lc + 32, t1);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 16; ++h) ls[h] = __uint_as_float(t0[h]) + __uint_as_float(t1[h]);
-              tmem_ld16(oc, t0);
-              tmem_ld16(oc + 32, t1);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 16; ++h) {                              // high part + low part
-                o[h] = __uint_as_float(t0[h]) + __uint_as_float(t1[h]);
-                if (whole) o[h] *= ls[h] > 0.f ? rcp_approx(ls[h]) : 0.f;
-              }
-              // row `row`, 4-head group c at group c ^ (row % 8): the column reads below then
-              // spread over 8 banks
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int cg = (hb >> 2) + c;
-                *reinterpret_cast<float4*>(scr + row * 32 + 4 * (cg ^ (row & 7))) =
-                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-              }
-              if (!whole && row == 0) {
-#pragma unroll
-                for (int h = 0; h < 16; ++h) red[32 + hb + h] = ls[h];
-              }
-            }
+            const uint32_t oc = tmem + lane_off + 64 + 64 * ob + hb;
+            uint32_t t0[16], t1[16];
+            float o[16];
+            tmem_ld16(oc, t0);
+            tmem_ld16(oc + 32, t1);
+            tmem_wait_ld();
             tc_fence_before();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {                              // high part + low part
+              o[h] = __uint_as_float(t0[h]) + __uint_as_float(t1[h]);
+              if (whole) o[h] *= ls[h] > 0.f ? rcp_approx(ls[h]) : 0.f;
+            }
+            // row `row`, 4-head group cg at group cg ^ (row % 8): the column reads below then
+            // spread over 8 banks
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int cg = 4 * gi + c;
+              *reinterpret_cast<float4*>(scr + row * 32 + 4 * (cg ^ (row & 7))) =
+                  make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            }
             if (!whole && row == 0) {
 #pragma unroll
-              for (int h = 0; h < 32; ++h) red[h] = m[h];
+              for (int h = 0; h < 16; ++h) {
+                red_m[hb + h] = m[h];
+                red_l[hb + h] = ls[h];
+              }
             }
           }
           __syncwarp();
           if (lane == 0 && !bad) mbar_arrive(&bar[BAR_OEMPTY + ob]);
-          named_bar(2, 128);
-          const int t128 = threadIdx.x - 64;
+          named_bar(6, 256);
+          const int tg = threadIdx.x - 128 - 128 * gi;                   // thread of the group
+          const int nh = a.G - hb < 16 ? a.G - hb : 16;                  // the group's heads
           if (!bad) {
-            const size_t qrow0 = (size_t)mt.s * a.n_h + (size_t)mt.g * a.G;
+            const size_t qrow0 = (size_t)mt.s * a.n_h + (size_t)mt.g * a.G + hb;
             const long long part = (long long)mt.s * a.n_kv + mt.g + p;
 #pragma unroll 4
-            for (int idx = t128; idx < a.G * 128; idx += 128) {
-              const int h = idx >> 7, c = idx & 127;
+            for (int idx = tg; idx < nh * 128; idx += 128) {
+              const int hh = idx >> 7, h = hb + hh, c = idx & 127;
               const float v = scr[c * 32 + 4 * ((h >> 2) ^ (c & 7)) + (h & 3)];
               if (!whole) a.ws_o[((size_t)part * a.G + h) * 128 + c] = v;
-              else if (a.out_f32) reinterpret_cast<float*>(a.out)[(qrow0 + h) * 128 + c] = v;
-              else reinterpret_cast<__nv_bfloat16*>(a.out)[(qrow0 + h) * 128 + c] = __float2bfloat16_rn(v);
+              else if (a.out_f32) reinterpret_cast<float*>(a.out)[(qrow0 + hh) * 128 + c] = v;
+              else reinterpret_cast<__nv_bfloat16*>(a.out)[(qrow0 + hh) * 128 + c] = __float2bfloat16_rn(v);
             }
-            if (!whole && t128 < a.G)
-              *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + t128) * 2) = make_float2(red[t128], red[32 + t128]);
+            if (!whole && tg < nh)
+              *reinterpret_cast<float2*>(a.ws_ml + ((size_t)part * a.G + hb + tg) * 2) =
+                  make_float2(red_m[hb + tg], red_l[hb + tg]);
           }
-          named_bar(2, 128);                 // the scratch is read before the next tile's P lands
+          named_bar(6, 256);                 // the scratch is read before the next tile's P lands
         }
         if (flags & F_END) break;
         ++i;
