@@ -166,8 +166,6 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
       int flags = 0;
       if (pj == 0 || cur.blk == 0) flags |= F_FIRST;
       if (end || lb == cur.nb - 1) flags |= F_LAST;
-      if (cur.blk == 0) flags |= F_SEGB;
-      if (lb == cur.nb - 1) flags |= F_SEGE;
       if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
       if (pair) flags |= F_PAIR;
       if (end) flags |= F_END;
@@ -241,7 +239,6 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
     const int4 mt = meta[slot];
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;   // first q head of the group
-    if (warp == 0 && lane == 0) record_pieces(a, (long long)s * a.n_kv + g, flags, p);
 
     if (flags & F_FIRST) {
 #pragma unroll
@@ -561,7 +558,7 @@ static pkv_status decode_bf16(const void* q, const void* k_pool, const void* v_p
   a.block_size = block_size;
   a.inline_plan = batch <= kInlinePlanSeqs;
   a.pieces = reinterpret_cast<int4*>(ws + wl.pieces);
-  a.seg_pp = reinterpret_cast<int2*>(ws + wl.segpp);
+  a.P_launch = v->P;
   a.batch = batch;
   a.n_h = n_h;
   a.n_kv = n_kv;

@@ -20,9 +20,6 @@ enum : int { F_FIRST = 1, F_LAST = 2, F_WHOLE = 4, F_VALID = 8 };
 // Ring stages of up to two blocks: F_PAIR marks a stage that also holds the next block of
 // the same segment; F_END marks the last stage of a piece.
 enum : int { F_PAIR = 16, F_END = 32 };
-// The stage holds the segment's first block (F_SEGB) / its last block (F_SEGE): the kernel
-// then records its piece as the first / last piece of the segment for the split-reduce.
-enum : int { F_SEGB = 64, F_SEGE = 128 };
 // Lazy softmax offset (base-2 units): the attention kernels raise a head's running offset
 // only when a score exceeds it by more than this, so exponentials stay below 2^8 (well
 // inside the range of the fp16 / bf16 high + low split of P) and most tiles skip the max
@@ -52,13 +49,11 @@ struct DecodeArgs {
   // INT4 cache (unused by the bf16 kernel): (block, kv head) records and the bf16 K tail
   const uint8_t* cache;
   const __nv_bfloat16* k_tail;
-  // workspace: [B * n_kv] (first piece, last piece) of every non-empty segment, written by
-  // the attention kernel on every call (equal when one piece holds the whole segment)
-  int2* seg_pp;
+  int P_launch;                  // CTAs of the attention grid (the reduce derives the pieces)
 };
 
 struct WorkspaceLayout {
-  size_t cum, ctx, pieces, segpp, ml, o, total;
+  size_t cum, ctx, pieces, ml, o, total;
 };
 
 // Pieces actually used for a line of W positions when P CTAs are launched: at least
@@ -78,8 +73,7 @@ __host__ inline WorkspaceLayout workspace_layout(int B, int n_kv, int G, int D, 
   w.cum = 0;
   w.ctx = align_up(sizeof(int32_t) * (size_t)(B + 1), 16);
   w.pieces = align_up(w.ctx + sizeof(int32_t) * (size_t)B, 32);
-  w.segpp = align_up(w.pieces + 2 * sizeof(int4) * (size_t)P, 16);
-  w.ml = align_up(w.segpp + sizeof(int2) * (size_t)B * n_kv, 256);
+  w.ml = align_up(w.pieces + 2 * sizeof(int4) * (size_t)P, 256);
   w.o = align_up(w.ml + sizeof(float) * parts * G * 2, 256);
   w.total = align_up(w.o + sizeof(float) * parts * G * D, 256);
   return w;
@@ -298,10 +292,6 @@ __device__ __forceinline__ void softmax_tile(float (&sc)[TT][NH][4], float (&m)[
 }
 
 // Records piece p as the first and / or last piece of segment seg (flags of the stage).
-__device__ __forceinline__ void record_pieces(const DecodeArgs& a, long long seg, int flags, int p) {
-  if (flags & F_SEGB) a.seg_pp[seg].x = p;
-  if (flags & F_SEGE) a.seg_pp[seg].y = p;
-}
 
 // Host launchers (decode_plan.cu).
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int block_size,

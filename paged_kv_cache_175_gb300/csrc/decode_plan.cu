@@ -165,36 +165,66 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int
 }
 
 // ---- reduce: merge the partial softmax states of segments split across pieces ----------------
-// One warp per (sequence, q head).  Segments that fit in one piece were finished by the
-// attention kernel itself; empty sequences get a zero row here.  The context length is
-// read before the grid-dependency wait (an input of the call, or the plan kernel's, which
-// finished before the attention kernel let this one launch), so that work overlaps the
-// attention kernel's tail; the pieces a segment spans come from the attention kernel.
+// One warp per (sequence, q head), eight per CTA.  The pieces a segment spans follow from
+// the partition alone (the line of blocks and the attention grid's size), so every warp
+// finds them before the grid-dependency wait: warps of segments that one piece holds
+// (finished by the attention kernel itself) leave without waiting, and after the wait the
+// others have one round of loads of the partial states left.  Empty sequences get a zero
+// row here.  Without a plan kernel the CTA first lays out the blocks of every sequence and
+// their prefix sums in shared memory (one sequence per thread); the context lengths are
+// inputs of the call, and the plan kernel's prefix sums finished before the attention
+// kernel let this one launch.
 template <int D>
-__global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
   constexpr int V = D / 32;                                   // channels per lane
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const bool live = row < a.batch * a.n_h;
-  int nb = 0;
-  long long seg = 0;
-  if (live) {
-    const int s = row / a.n_h, h = row % a.n_h;
-    const int ctx = a.inline_plan ? clamp_ctx(a.ctx_raw[s], a.max_ctx) : a.ctx_eff[s];
-    nb = span_blocks(ctx, a.window, a.block_size);
-    seg = (long long)s * a.n_kv + h / a.G;
+  static_assert(kInlinePlanSeqs == 8 * 32, "one sequence per thread of the CTA");
+  __shared__ int snb[kInlinePlanSeqs], spre[kInlinePlanSeqs], schunk[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  if (a.inline_plan) {
+    // blocks of every sequence and their exclusive prefix: thread t takes sequence t
+    const int sq = threadIdx.x;
+    const int n = sq < a.batch ? span_blocks(clamp_ctx(a.ctx_raw[sq], a.max_ctx), a.window, a.block_size) : 0;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) schunk[warp] = incl;
+    __syncthreads();
+    int carry = 0;
+    for (int c = 0; c < warp; ++c) carry += schunk[c];
+    snb[sq] = n;
+    spre[sq] = carry + incl - n;
+    __syncthreads();
   }
-  grid_dep_wait();
-  if (!live) return;
-  const int hl = (row % a.n_h) % a.G;
+  if (row >= a.batch * a.n_h) return;
+  const int s = row / a.n_h, hq = row % a.n_h, g = hq / a.G, hl = hq % a.G;
+  const long long seg = (long long)s * a.n_kv + g;
+  long long before, total;                                    // blocks of sequences < s, of all
+  int nb;
+  if (a.inline_plan) {
+    before = spre[s];
+    total = 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) total += schunk[c];
+    nb = snb[s];
+  } else {
+    before = a.cum[s];
+    total = a.cum[a.batch];
+    nb = a.cum[s + 1] - a.cum[s];
+  }
   int p0 = 0, p1 = 0;
   if (nb > 0) {
-    // the first and last pieces of the segment, recorded by the attention kernel
-    const int2 pp = a.seg_pp[seg];
-    if (pp.x == pp.y) return;                                 // finished by the attention kernel
-    p0 = pp.x;
-    p1 = pp.y;
+    const long long W = (long long)a.n_kv * total;
+    const int P = effective_pieces(W, a.P_launch);
+    const long long start = (long long)a.n_kv * before + (long long)g * nb;
+    p0 = piece_of(start, W, P);
+    p1 = piece_of(start + nb - 1, W, P);
+    if (p0 == p1) return;                                     // finished by the attention kernel
   }
+  grid_dep_wait();
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
@@ -267,7 +297,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const DecodeArgs a) {
 cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream) {
   const int rows = a.batch * a.n_h;
   if (rows == 0) return cudaSuccess;
-  dim3 grid((rows + 3) / 4), block(128);
+  dim3 grid((rows + 7) / 8), block(256);
   DecodeArgs args = a;
   (void)P;
   void* kargs[] = {&args};

@@ -153,8 +153,6 @@ __global__ void __launch_bounds__(384, 1)
         if (seg_last || end) flags |= F_LAST;
         if (cur.seg_start >= pstart && cur.seg_start + cur.nb <= pend) flags |= F_WHOLE;
         if (end) flags |= F_END;
-        if (cur.blk == 0) flags |= F_SEGB;
-        if (seg_last) flags |= F_SEGE;
         const int32_t* row = a.bt + (size_t)cur.s * a.max_blocks + cur.b0;
         t.phys = lane < nblk ? __ldg(row + cur.blk + lane) : -1;
         if (lane == 0 && cur.blk + 2 * NBT < cur.nb) prefetch_l2(row + cur.blk + 2 * NBT);
@@ -347,7 +345,6 @@ __global__ void __launch_bounds__(384, 1)
         }
         const TcTileMeta mt = vmeta[slot];
         const int ntok = mt.rows & 255, flags = (mt.rows >> 8) & 255, lead = mt.rows >> 16, ob = mt.k & 1;
-        if (threadIdx.x == 128) record_pieces(a, (long long)mt.s * a.n_kv + mt.g, flags, p);
         tc_fence_after();
         float x[16];
         {

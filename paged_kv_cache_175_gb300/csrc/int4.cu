@@ -536,8 +536,7 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
     const bool ok = (unsigned)phys < (unsigned)a.num_blocks && (!pair || (unsigned)phys1 < (unsigned)a.num_blocks);
     const bool go = ok && ok_wait, end = pj + nblk >= len;
     const int flags = (seg_rows >> 8 & F_WHOLE) | (ok ? F_VALID : 0) | (first ? F_FIRST : 0) |
-                      (last || end ? F_LAST : 0) | (pair ? F_PAIR : 0) | (end ? F_END : 0) |
-                      (cur.blk == 0 ? F_SEGB : 0) | (last ? F_SEGE : 0);
+                      (last || end ? F_LAST : 0) | (pair ? F_PAIR : 0) | (end ? F_END : 0);
     if (lane == 0) {
       if (!ok_wait) {
         set_err(a.err, PKV_DEV_TIMEOUT);
@@ -598,7 +597,6 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
     // ntok, lead: the stage's attended rows are [lead, ntok) of its TT * 16
     const int s = mt.x, g = mt.y, ntok = mt.w & 255, flags = (mt.w >> 8) & 255, lead = mt.w >> 16;
     const size_t qrow0 = (size_t)s * a.n_h + (size_t)g * a.G;
-    if (warp == 0 && lane == 0) record_pieces(a, (long long)s * a.n_kv + g, flags, p);
 
     if (flags & F_FIRST) {
 #pragma unroll
@@ -1084,7 +1082,7 @@ static pkv_status decode_int4(const void* q, const uint8_t* cache, const void* k
   a.block_size = block_size;
   a.inline_plan = batch <= kInlinePlanSeqs;
   a.pieces = reinterpret_cast<int4*>(ws + wl.pieces);
-  a.seg_pp = reinterpret_cast<int2*>(ws + wl.segpp);
+  a.P_launch = vv->P;
   a.batch = batch;
   a.n_h = n_h;
   a.n_kv = n_kv;
