@@ -33,32 +33,44 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
   }
 }
 
-// A CTA takes BPC consecutive listed blocks (so a CTA moves at least ~32 KB even when one
-// block is a few KB).  Angles delta * inv_freq[j] are formed in fp64 and reduced to
-// [-pi, pi] in fp64 (k = rint(angle / 2pi), taken as a product with 1 / 2pi), and only the
-// reduced angle goes to the fp32 sincos, so large position deltas keep full fp32 accuracy.
-// A block whose delta equals its predecessor's in the CTA reuses its table (the blocks of a
-// reused chunk share one delta).  The rotation runs in fp32 on bf16 pairs and stores with
+// The listed blocks' rows are cut into equal ranges of ipc items (an item: one 16-byte
+// vector of each half of a row, 32 bytes), about 32 KB per CTA: several consecutive listed
+// blocks when blocks are small, part of one (or of two) when they are large.  Every thread
+// issues all of its loads (NI items) before the angle tables are built, so the loads and
+// the fp64 / sincos work overlap and a CTA needs one memory round trip.  Angles
+// delta * inv_freq[j] are formed in fp64 and reduced to [-pi, pi] in fp64
+// (k = rint(angle / 2pi), taken as a product with 1 / 2pi), and only the reduced angle goes
+// to the fp32 sincos, so large position deltas keep full fp32 accuracy.  A block whose
+// delta equals its predecessor's in the CTA reuses its table (the blocks of a reused chunk
+// share one delta).  The rotation runs in fp32 on bf16 pairs and stores with
 // round-to-nearest-even.
 struct RopeFreq {
   double inv_freq[64];
 };
-constexpr int kRopeMaxBPC = 8;
+constexpr int kRopeMaxBPC = 8;      // blocks a CTA's range may touch
+constexpr int kRopeNI = 4;          // items per thread and round (64 registers: 4 CTAs per SM)
 
 template <int D>
-__global__ void __launch_bounds__(256) rope_shift_kernel(__nv_bfloat16* __restrict__ k_pool,
+__global__ void __launch_bounds__(256, 4) rope_shift_kernel(__nv_bfloat16* __restrict__ k_pool,
                                                          const int32_t* __restrict__ block_ids,
                                                          const int32_t* __restrict__ deltas, int n_blocks,
-                                                         int num_blocks, int n_kv, int block_size, int bpc,
+                                                         int num_blocks, int n_kv, int block_size, int ipc,
                                                          const RopeFreq f, int32_t* err) {
   constexpr int H = D / 2;
+  constexpr int V = H / 8;                                    // vectors per half row
+  constexpr int NI = kRopeNI;
   __shared__ float cs[kRopeMaxBPC][H], sn[kRopeMaxBPC][H];
   __shared__ int tab[kRopeMaxBPC];                           // table of each block slot
   __shared__ int phys_s[kRopeMaxBPC], delta_s[kRopeMaxBPC];
-  const int b0 = blockIdx.x * bpc;
-  const int nb = n_blocks - b0 < bpc ? n_blocks - b0 : bpc;
+  const int rows = n_kv * block_size;
+  const long long ipb = (long long)rows * V;                 // items per block
+  const long long i0 = (long long)blockIdx.x * ipc;
+  const long long i1 = i0 + ipc < (long long)n_blocks * ipb ? i0 + ipc : (long long)n_blocks * ipb;
+  const int b_first = (int)(i0 / ipb);
+  const int nb = (int)((i1 - 1) / ipb) - b_first + 1;         // <= kRopeMaxBPC (host sizes ipc)
+  const int total = (int)(i1 - i0);
   if (threadIdx.x < nb) {
-    const int ph = block_ids[b0 + threadIdx.x], dl = deltas[b0 + threadIdx.x];
+    const int ph = block_ids[b_first + threadIdx.x], dl = deltas[b_first + threadIdx.x];
     const bool okb = (unsigned)ph < (unsigned)num_blocks;
     if (!okb) set_err(err, PKV_DEV_BAD_BLOCK);
     phys_s[threadIdx.x] = okb ? ph : -1;
@@ -68,28 +80,26 @@ __global__ void __launch_bounds__(256) rope_shift_kernel(__nv_bfloat16* __restri
   if (threadIdx.x == 0) {
     for (int b = 0; b < nb; ++b) tab[b] = (b > 0 && delta_s[b] == delta_s[b - 1]) ? tab[b - 1] : b;
   }
-  const int rows = n_kv * block_size;
-  // one 16-byte vector of each half of a row per item: channels j0..j0+7 and their partners
-  constexpr int V = H / 8;                                    // vectors per half row
-  constexpr int NI = 4;                                       // items in flight per thread
-  const int per_block = rows * V, total = nb * per_block;
-  // the first items' keys are loaded before the angle tables are built, so the loads and the
-  // fp64 / sincos work overlap
+  const int off0 = (int)(i0 - (long long)b_first * ipb);     // first item's place in block b_first
   uint4 av[NI], bv[NI];
-  uint4* rp[NI];
+  unsigned live = 0;                                          // bit k: item k of the round is rotated
+  // address of the first vector of an item: row r of the block, vector rem % V of its first half
+  auto item_ptr = [&](int flat) -> uint4* {
+    const int b = flat / (int)ipb, rem = flat - b * (int)ipb, r = rem / V;
+    return reinterpret_cast<uint4*>(k_pool + ((size_t)phys_s[b] * rows + r) * D) + (rem - r * V);
+  };
   auto load = [&](int base) {
+    live = 0;
 #pragma unroll
     for (int k = 0; k < NI; ++k) {
       const int idx = base + k * blockDim.x;
-      rp[k] = nullptr;
       if (idx < total) {
-        const int b = idx / per_block, rem = idx - b * per_block;
-        const int phys = phys_s[b];
-        if (phys >= 0 && delta_s[b] != 0) {                  // else a bad id (flagged) or the identity
-          const int r = rem / V;
-          rp[k] = reinterpret_cast<uint4*>(k_pool + ((size_t)phys * rows + r) * D) + (rem - r * V);
-          av[k] = rp[k][0];
-          bv[k] = rp[k][V];
+        const int flat = off0 + idx, b = flat / (int)ipb;
+        if (phys_s[b] >= 0 && delta_s[b] != 0) {             // else a bad id (flagged) or the identity
+          const uint4* p = item_ptr(flat);
+          av[k] = p[0];
+          bv[k] = p[V];
+          live |= 1u << k;
         }
       }
     }
@@ -111,9 +121,9 @@ __global__ void __launch_bounds__(256) rope_shift_kernel(__nv_bfloat16* __restri
   for (int base = threadIdx.x;; base += NI * blockDim.x) {
 #pragma unroll
     for (int k = 0; k < NI; ++k) {
-      if (!rp[k]) continue;
-      const int idx = base + k * blockDim.x;
-      const int b = idx / per_block, rem = idx - b * per_block;
+      if (!((live >> k) & 1)) continue;
+      const int flat = off0 + base + k * blockDim.x;
+      const int b = flat / (int)ipb, rem = flat - b * (int)ipb;
       const float* c = cs[tab[b]];
       const float* sr = sn[tab[b]];
       const int j0 = 8 * (rem % V);
@@ -128,8 +138,9 @@ __global__ void __launch_bounds__(256) rope_shift_kernel(__nv_bfloat16* __restri
       rot(av[k].y, bv[k].y, j0 + 2);
       rot(av[k].z, bv[k].z, j0 + 4);
       rot(av[k].w, bv[k].w, j0 + 6);
-      rp[k][0] = av[k];
-      rp[k][V] = bv[k];
+      uint4* p = item_ptr(flat);
+      p[0] = av[k];
+      p[V] = bv[k];
     }
     if (base + NI * blockDim.x >= total) break;
     load(base + NI * blockDim.x);
@@ -182,20 +193,26 @@ extern "C" pkv_status pkv_rope_shift_k(void* k_pool, const int32_t* block_ids, c
   RopeFreq f = {};
   for (int j = 0; j < head_dim / 2; ++j) f.inv_freq[j] = std::pow(rope_base, -2.0 * j / head_dim);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // consecutive listed blocks per CTA: about 32 KB of keys per CTA, at most kRopeMaxBPC
-  const long long block_bytes = (long long)n_kv * block_size * head_dim * 2;
-  int bpc = (int)((32768 + block_bytes - 1) / block_bytes);
-  bpc = bpc < 1 ? 1 : (bpc > kRopeMaxBPC ? kRopeMaxBPC : bpc);
-  // one thread per 16-byte vector pair, at most 256 (they loop), at least 64
-  const long long items = (long long)bpc * n_kv * block_size * (head_dim / 16);
-  const int threads = items >= 256 ? 256 : (items <= 64 ? 64 : (int)((items + 31) / 32 * 32));
-  const unsigned grid = (unsigned)((n_blocks + bpc - 1) / bpc);
+  // ranges of about 32 KB (1024 items) per CTA: a whole number of blocks, at most
+  // kRopeMaxBPC, when blocks are smaller, else 1024 items (then a range touches at most two
+  // blocks); 256 threads of kRopeNI items each, fewer for a smaller range
+  const long long ipb = (long long)n_kv * block_size * (head_dim / 16);
+  long long ipc = 1024;
+  if (ipb < 1024) {
+    long long k = 1024 / ipb;
+    k = k > kRopeMaxBPC ? kRopeMaxBPC : k;
+    ipc = k * ipb;
+  }
+  const long long need = (ipc + kRopeNI - 1) / kRopeNI;
+  const int threads = need >= 256 ? 256 : (int)((need + 31) / 32 * 32);
+  const long long all = (long long)n_blocks * ipb;
+  const unsigned grid = (unsigned)((all + ipc - 1) / ipc);
   if (head_dim == 128)
     rope_shift_kernel<128><<<grid, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
-                                                     n_blocks, num_blocks, n_kv, block_size, bpc, f, err_flag);
+                                                     n_blocks, num_blocks, n_kv, block_size, (int)ipc, f, err_flag);
   else
     rope_shift_kernel<64><<<grid, threads, 0, st>>>(static_cast<__nv_bfloat16*>(k_pool), block_ids, deltas,
-                                                    n_blocks, num_blocks, n_kv, block_size, bpc, f, err_flag);
+                                                    n_blocks, num_blocks, n_kv, block_size, (int)ipc, f, err_flag);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);

@@ -64,7 +64,10 @@ def _close_ulps(got, ref, ulps):
     return bool((d <= tol).all()), float((d / np.maximum(bf16_ulp(ref), 1e-30)).max())
 
 
-@pytest.mark.parametrize("D,BS,n_kv", [(64, 16, 2), (128, 16, 1), (128, 32, 32)])
+# a CTA takes about 32 KB of rows: several small blocks (capped at 8 for the smallest),
+# part of one large block, or ranges that straddle two blocks (9 and 5 kv heads)
+@pytest.mark.parametrize("D,BS,n_kv", [(64, 16, 2), (64, 16, 1), (128, 16, 1), (128, 32, 32), (128, 16, 9),
+                                       (64, 64, 5)])
 def test_rope_shift_matches_oracle(D, BS, n_kv):
     kp, ids, deltas = _rope_case(D, BS, n_kv, seed=D + n_kv)
     ref = oracle.rope_shift_k(f64(kp), ids, deltas)
