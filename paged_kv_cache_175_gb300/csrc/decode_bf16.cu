@@ -66,7 +66,8 @@ __global__ void __launch_bounds__((MT + (PW ? 1 : 0)) * 32,
   constexpr int MD = D / 16;        // 16-channel m-tiles of O^T
   constexpr int HW = 8 * NH;        // heads per warp
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by an offset from the array itself, so every access stays a shared-memory one
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = a.stages;
   int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * SST);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + S);

@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(384, 1)
   using L = TcLayout<BS>;
   constexpr int NBT = L::NBT;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by an offset from the array itself, so every access stays a shared-memory one
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   TcTileMeta* kmeta = reinterpret_cast<TcTileMeta*>(sm + L::M_OFF);   // per K stage
   TcTileMeta* vmeta = kmeta + L::NK;                                    // per V stage
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::M_OFF + L::META);

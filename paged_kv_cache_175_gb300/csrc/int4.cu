@@ -422,7 +422,8 @@ __global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 &
   constexpr int CV = D / 8;         // V channels per thread (rows of the V^T fragments)
   constexpr int VW = CV / 8;        // V code words per thread per token row
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // aligned by an offset from the array itself, so every access stays a shared-memory one
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int S = a.stages;
   int4* meta = reinterpret_cast<int4*>(smem + (size_t)S * SST);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + S);
