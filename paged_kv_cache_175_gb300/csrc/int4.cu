@@ -408,7 +408,7 @@ __device__ __forceinline__ void softmax_tile_c(float (&sc)[TT][NH][4], float (&m
 // softmax work is shared by twice the tokens).  COMB: groups of up to 4 heads, high and
 // low parts of the folded operands in the two halves of one 8-head n-tile.
 template <int D, int BS, int NH, int MT, int TB, bool COMB>
-__global__ void __launch_bounds__(MT * 32, TB == 2 ? 12 : (BS == 16 && MT == 1 && NH == 1 ? 16 : 0))
+__global__ void __launch_bounds__(MT * 32, TB == 2 || (BS == 64 && MT == 1) ? 12 : (BS == 16 && MT == 1 && NH == 1 ? 16 : 0))
     decode_int4_kernel(const DecodeArgs a) {
   using T = Int4Tile<D, BS>;
   constexpr int TPB = BS / 16;      // 16-token tiles per block
