@@ -167,9 +167,9 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int
 // ---- reduce: merge the partial softmax states of segments split across pieces ----------------
 // One warp per (sequence, q head), eight per CTA.  The pieces a segment spans follow from
 // the partition alone (the line of blocks and the attention grid's size), so every warp
-// finds them before the grid-dependency wait: warps of segments that one piece holds
-// (finished by the attention kernel itself) leave without waiting, and after the wait the
-// others have one round of loads of the partial states left.  Empty sequences get a zero
+// finds them before the grid-dependency wait, and after the wait the warps of segments
+// cut by piece boundaries have one round of loads of the partial states left (those of
+// segments that one piece holds, finished by the attention kernel itself, leave).  Empty sequences get a zero
 // row here.  Without a plan kernel the CTA first lays out the blocks of every sequence and
 // their prefix sums in shared memory (one sequence per thread); the context lengths are
 // inputs of the call, and the plan kernel's prefix sums finished before the attention
@@ -199,7 +199,13 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
     spre[sq] = carry + incl - n;
     __syncthreads();
   }
-  if (row >= a.batch * a.n_h) return;
+  // Every thread passes the grid-dependency wait, also those with nothing to do: this grid
+  // then completes only after the attention kernel, so no launch after it on the stream
+  // can overlap that kernel.
+  if (row >= a.batch * a.n_h) {
+    grid_dep_wait();
+    return;
+  }
   const int s = row / a.n_h, hq = row % a.n_h, g = hq / a.G, hl = hq % a.G;
   const long long seg = (long long)s * a.n_kv + g;
   long long before, total;                                    // blocks of sequences < s, of all
@@ -222,9 +228,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
     const long long start = (long long)a.n_kv * before + (long long)g * nb;
     p0 = piece_of(start, W, P);
     p1 = piece_of(start + nb - 1, W, P);
-    if (p0 == p1) return;                                     // finished by the attention kernel
   }
   grid_dep_wait();
+  if (nb > 0 && p0 == p1) return;                             // finished by the attention kernel
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
