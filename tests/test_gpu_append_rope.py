@@ -124,3 +124,24 @@ def test_rope_full_size_sampled(name):
     ref = oracle.rope_shift_k(before, np.arange(len(pick)), deltas[pick])
     ok, worst = _close_ulps(after, ref, 2)
     assert ok, worst
+
+
+@pytest.mark.parametrize("D,BS,n_kv", [(128, 16, 1), (128, 16, 9)])
+def test_rope_bad_block_inside_a_range_is_skipped(D, BS, n_kv):
+    # a bad id among listed blocks that share a CTA's range (small blocks) or whose ranges
+    # straddle block edges (9 kv heads): the bad block is flagged and skipped, every other
+    # listed block is rotated as the oracle rotates it
+    kp, ids, deltas = _rope_case(D, BS, n_kv, seed=77 + n_kv)
+    bad = ids.copy()
+    bad[5] = kp.shape[0] + 3
+    keep = np.array([i for i in range(len(ids)) if i != 5])
+    ref = oracle.rope_shift_k(f64(kp), ids[keep], deltas[keep])
+    kd = kp.to(DEV)
+    err = err_flag()
+    pkv.rope_shift_k(kd, torch.as_tensor(bad, device=DEV), torch.as_tensor(deltas, device=DEV), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pkv.DEV_BAD_BLOCK
+    ok, worst = _close_ulps(f64(kd), ref, 2)
+    assert ok, worst
+    untouched = np.setdiff1d(np.arange(kp.shape[0]), ids[keep][1:])
+    assert np.array_equal(_bits(kd)[untouched], _bits(kp)[untouched])
