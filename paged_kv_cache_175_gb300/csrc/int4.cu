@@ -15,6 +15,7 @@ __host__ __device__ constexpr int channel_of(int n) { return n < 4 ? 2 * n : 2 *
 
 struct GroupQuant {
   float s, m;           // fp16 scale / min, widened
+  float r;              // 1 / s rounded to nearest (0 when s is 0)
   __half s16, m16;
 };
 
@@ -28,12 +29,21 @@ __device__ __forceinline__ GroupQuant group_params(float lo, float hi) {
   q.m16 = __float2half_rn(lo);
   q.s = __half2float(q.s16);
   q.m = __half2float(q.m16);
+  q.r = q.s == 0.f ? 0.f : __frcp_rn(q.s);
   return q;
 }
-// Step (4): code of one value.
+// Step (4): code of one value, rint((x - m) / s) with the quotient rounded to nearest,
+// clamped to [0, 15].  Where the clamp does not decide the code, |quotient| <= 16, and the
+// product with the rounded reciprocal is then within 3e-6 of the rounded quotient (each is
+// within 2^-23 relative of the exact one); so when the product lies more than 1e-5 from
+// every half-integer both round to the same integer, and only near a tie is the division
+// itself taken.  NaN and infinite inputs give the same codes either way.
 __device__ __forceinline__ uint32_t quant_code(float x, const GroupQuant& q) {
   if (q.s == 0.f) return 0u;
-  float c = rintf(__fdiv_rn(__fsub_rn(x, q.m), q.s));
+  const float d = __fsub_rn(x, q.m);
+  const float t = __fmul_rn(d, q.r);
+  float c = rintf(t);
+  if (fabsf(fabsf(t - c) - 0.5f) < 1e-5f) c = rintf(__fdiv_rn(d, q.s));
   c = fminf(fmaxf(c, 0.f), 15.f);
   return (uint32_t)c;
 }

@@ -171,3 +171,29 @@ def test_full_size_sampled(name):
         check_attention(out[s:s + 1], refo, f"{name} seq {s} ctx {int(w.context_lens[s])}", min_exact=0.95)
         check_attention(out32[s:s + 1], refo, f"{name} seq {s} fp32",
                         f32_bars=(BAR_INT4_F32_MAXABS, BAR_INT4_F32_RELL2))
+
+
+@pytest.mark.parametrize("D,BS", [(128, 16), (64, 32)])
+def test_codes_on_exact_ties_round_half_to_even(D, BS):
+    # Every group spans [0, 7.5] exactly, so s = 0.5 and min = 0 are exact in fp16 and every
+    # other value 0.25 + 0.5 k sits exactly on a tie (quotient k + 0.5): the codes must be the
+    # oracle's round-half-to-even of the exact quotient, with ties mixed among ordinary values
+    rng = np.random.default_rng(D + BS)
+    n_kv = 2
+    def grid(shape):
+        x = 0.25 + 0.5 * rng.integers(0, 15, size=shape)
+        plain = rng.random(shape) < 0.3
+        x[plain] = 0.5 * rng.integers(0, 16, size=plain.sum())     # exact codes, no tie
+        return x
+    k = grid((BS, n_kv, D))
+    k[0], k[1] = 0.0, 7.5                                  # each channel's K range over the block
+    v = grid((BS, n_kv, D))
+    v[:, :, 0], v[:, :, 1] = 0.0, 7.5                      # each token's V range
+    k, v = torch.tensor(k).to(torch.bfloat16), torch.tensor(v).to(torch.bfloat16)
+    assert torch.equal(k.double(), torch.tensor(k.double().numpy()))   # all values exact in bf16
+    num_blocks = 3
+    cache = pkv.alloc_int4_cache(num_blocks, n_kv, BS, D, 1, DEV)
+    ref = oracle.Int4Cache(num_blocks, n_kv, BS, D, 1)
+    slots = np.arange(BS, dtype=np.int64) + BS                        # block 1, all rows
+    _append_both(cache, ref, k, v, slots, np.zeros(BS, np.int32))
+    _compare_state(cache, ref, [1], [0])
