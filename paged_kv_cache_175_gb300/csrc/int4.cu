@@ -72,23 +72,29 @@ struct QuantAppendArgs {
   int32_t* err;
 };
 
-// Phase 1: one warp per (token, kv head).  V is quantized per token; a token that fills
-// the last row of its block also quantizes that block's K per channel, taking rows
-// appended earlier in this call from `k` and older rows from the tail.
+// Phase 1: D / 32 warps per (token, kv head).  The first quantizes V per token; when the
+// token fills the last row of its block, each of them quantizes 32 of that block's K
+// channels (per channel), taking rows appended earlier in this call from `k` and older rows
+// from the tail.
+template <int D>
+constexpr int kKWarps = D / 32;                 // warps per (token, kv head)
 template <int D, int BS>
 __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs a) {
   grid_dep_launch();                            // the tail update may launch; it waits for this grid
   constexpr int CPL = D / 32;                   // V channels per lane
   constexpr int LPW = 8 / CPL;                  // lanes per 32-bit code word
+  constexpr int KQ = kKWarps<D>;
   const int lane = threadIdx.x & 31;
-  const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long wall = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long wid = wall / KQ;
+  const int kq = (int)(wall - wid * KQ);        // this warp's 32 K channels: [32 kq, 32 kq + 32)
   if (wid >= (long long)a.n_tok * a.n_kv) return;
   const int i = (int)(wid / a.n_kv), g = (int)(wid % a.n_kv);
   const long long slot = a.slots[i];
   if (slot < 0) return;
   const int seq = a.tail_seq[i];
   if (slot >= a.n_slots || (unsigned)seq >= (unsigned)a.tail_rows) {
-    if (lane == 0 && g == 0) set_err(a.err, PKV_DEV_BAD_SLOT);
+    if (lane == 0 && g == 0 && kq == 0) set_err(a.err, PKV_DEV_BAD_SLOT);
     return;
   }
   const long long blk = slot / BS;
@@ -97,7 +103,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
   uint8_t* rec = a.cache + tile * a.rec_bytes;            // K codes, V codes, K meta, V meta
 
   // ---- V: per token ----
-  {
+  if (kq == 0) {
     const __nv_bfloat16* src = a.v + ((size_t)i * a.n_kv + g) * D + lane * CPL;
     float x[CPL];
 #pragma unroll
@@ -147,16 +153,16 @@ __global__ void __launch_bounds__(256) quant_append_kernel(const QuantAppendArgs
   const __nv_bfloat16* krow_tail = a.k_tail + ((size_t)seq * a.n_kv + g) * BS * D;
   __half* kmeta = reinterpret_cast<__half*>(rec + (size_t)BS * D);
   uint32_t* kcodes = reinterpret_cast<uint32_t*>(rec);
-  // Lane (octet, row group): channels [8 octet, 8 octet + 8) -- one code word per row -- of
-  // the rows r0 + rg + RG k of each chunk of KR rows, loaded as 16-byte vectors, every load
-  // of a chunk issued before any is used.  The channel range comes from a min / max over the
-  // lane's rows and then across the row groups; a block of KR rows stays in registers from
-  // the range pass to the code pass.
-  constexpr int OCT = D / 8;                                 // channel octets
+  // Lane (octet, row group): channels [8 octet, 8 octet + 8) of this warp's 32 -- one code
+  // word per row -- of the rows r0 + rg + RG k of each chunk of KR rows, loaded as 16-byte
+  // vectors, every load of a chunk issued before any is used.  The channel range comes from
+  // a min / max over the lane's rows and then across the row groups; a block of KR rows
+  // stays in registers from the range pass to the code pass.
+  constexpr int OCT = 4;                                     // channel octets per warp
   constexpr int RG = 32 / OCT;                               // row groups
   constexpr int KR = 16;                                     // rows per chunk
   constexpr int RPL = KR / RG;                               // rows per lane and chunk
-  const int oct = lane % OCT, rg = lane / OCT;
+  const int oct = kq * OCT + lane % OCT, rg = lane / OCT;     // oct: octet within the row
   auto row_ptr = [&](int r) -> const __nv_bfloat16* {
     return r >= first_call_row ? krow_call + (size_t)(i - (BS - 1 - r)) * a.n_kv * D : krow_tail + (size_t)r * D;
   };
@@ -1038,7 +1044,8 @@ extern "C" pkv_status pkv_kv_quant_append_int4(const void* k, const void* v, con
   a.err = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long long warps = (long long)n_tok * n_kv;
-  const unsigned g1 = (unsigned)((warps * 32 + 255) / 256);
+  const long long qwarps = warps * (head_dim / 32);              // kKWarps per (token, kv head)
+  const unsigned g1 = (unsigned)((qwarps * 32 + 255) / 256);
   const long long vecs = warps * (head_dim / 8);
   const unsigned g2 = (unsigned)((vecs + 255) / 256);
 #define PKV_Q(d, b) \
