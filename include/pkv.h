@@ -186,7 +186,9 @@ int pkv_layer_window(const int32_t* windows, int n, int layer);
  *   lo, hi = fp32 min / max of the group (a zero lo is taken as +0);
  *   s32 = (hi - lo) / 15 (fp32, nearest);
  *   s16 = fp16(s32), m16 = fp16(lo) (nearest even);
- *   code = clamp(rint_half_even((x - m16) / s16), 0, 15) (fp32 subtract / divide),
+ *   code = clamp(rint_half_even((x - m16) / s16), 0, 15) (fp32 subtract / divide; the
+ *     kernel takes the quotient from the rounded reciprocal away from ties, which gives the
+ *     same codes),
  *   code = 0 when s16 == 0; the dequantized value is x^ = code * s16 + m16, exact.
  * Groups: V = the head_dim channels of one (token, kv head); K = one channel of one
  * (block, kv head) over the block's block_size rows.  K rows of a block that is not

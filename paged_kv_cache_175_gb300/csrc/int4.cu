@@ -1,5 +1,6 @@
-// INT4 paged KV cache: quantize-on-append and decode attention with in-register
-// dequantization.  Format and exact quantizer op sequence are documented in pkv.h.
+// INT4 paged KV cache: quantize-on-append, and decode attention over the exact codes with
+// the scales folded into the other operands.  Format and exact quantizer op sequence are
+// documented in pkv.h.
 #include <cmath>
 #include <mutex>
 
