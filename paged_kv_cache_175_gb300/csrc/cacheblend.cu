@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(kSelThreads)
   base = total;
   if (k == 0) return;
   const float* d = dev + lo;
+  // a segment of at most one key per thread keeps its keys in registers for every pass
+  const bool held = n <= kSelThreads;
+  const unsigned long long mine = held && (int)threadIdx.x < n ? sel_key(d, threadIdx.x) : 0ull;
   unsigned long long thresh = 0;                               // keys >= thresh are selected
   if (k < n) {
     // most significant byte first: find the byte of the k-th largest key, pass by pass;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kSelThreads)
       for (int j = threadIdx.x; j < 256; j += kSelThreads) hist[j] = 0;
       __syncthreads();
       for (int i = threadIdx.x; i < n; i += kSelThreads) {
-        const unsigned long long key = sel_key(d, i);
+        const unsigned long long key = held ? mine : sel_key(d, i);
         if ((key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
       }
       __syncthreads();
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(kSelThreads)
   int written = 0;
   for (int c0 = 0; c0 < n; c0 += kSelThreads) {
     const int i = c0 + threadIdx.x;
-    const int f = (i < n && (k == n || sel_key(d, i) >= thresh)) ? 1 : 0;
+    const int f = (i < n && (k == n || (held ? mine : sel_key(d, i)) >= thresh)) ? 1 : 0;
     const int pos = cta_exclusive_scan(f, warp_tot, &total);
     if (f) out[base + written + pos] = lo + i;
     written += total;
