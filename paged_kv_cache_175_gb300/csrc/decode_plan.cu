@@ -165,22 +165,85 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int
 }
 
 // ---- reduce: merge the partial softmax states of segments split across pieces ----------------
-// One warp per (sequence, q head), eight per CTA.  The pieces a segment spans follow from
-// the partition alone (the line of blocks and the attention grid's size), so every warp
-// finds them before the grid-dependency wait, and after the wait the warps of segments
-// cut by piece boundaries have one round of loads of the partial states left (those of
-// segments that one piece holds, finished by the attention kernel itself, leave).  Empty sequences get a zero
-// row here.  Without a plan kernel the CTA first lays out the blocks of every sequence and
-// their prefix sums in shared memory (one sequence per thread); the context lengths are
-// inputs of the call, and the plan kernel's prefix sums finished before the attention
-// kernel let this one launch.
+// The pieces a segment spans follow from the partition alone (the line of blocks and the
+// attention grid's size), so every thread finds them before the grid-dependency wait, and
+// the rows of segments that one piece holds (finished by the attention kernel itself) leave
+// right after it.  Empty sequences get a zero row here.  Without a plan kernel the CTA first
+// lays out the blocks of every sequence and their prefix sums in shared memory (one sequence
+// per thread); the context lengths are inputs of the call, and the plan kernel's prefix sums
+// finished before the attention kernel let this one launch.
+//
+// Two shapes.  Narrow: one warp per (sequence, q head), eight rows per CTA, for batches whose
+// segments span few pieces.  Wide: one CTA per row whose eight warps take interleaved chunks
+// of its pieces and combine their eight states through shared memory, for few long
+// sequences, where a segment spans a large share of the grid's pieces and one warp would
+// take one memory round trip per eight of them.
+
+// Pieces one warp loads at a time in merge_pieces.
+constexpr int kMergeChunk = 8;
+
+// Merges the states of pieces first, first+1, ... (chunks of CH taken every `step` pieces,
+// none past p1) of one (segment, head) into the running (M, L, acc), base-2 exponents.  Every
+// load of a chunk is issued before any is used, and chunks merge online.
 template <int D>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, long long seg, int hl, int lane, int first,
+                                             int p1, int step, float& M, float& L, float (&acc)[D / 32]) {
+  constexpr int V = D / 32, CH = kMergeChunk;
+  for (int pc = first; pc <= p1; pc += step) {
+    float mv[CH], lv[CH], ov[CH][V];
+    bool use[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int p = pc + i;
+      use[i] = p <= p1;
+      mv[i] = -INFINITY;
+      lv[i] = 0.f;
+#pragma unroll
+      for (int k = 0; k < V; ++k) ov[i][k] = 0.f;
+      if (use[i]) {
+        const long long part = (seg + p) * a.G + hl;
+        const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + part * 2);
+        mv[i] = ml.x;
+        lv[i] = ml.y;
+        const float* src = a.ws_o + part * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          ov[i][0] = v.x; ov[i][1] = v.y; ov[i][2] = v.z; ov[i][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          ov[i][0] = v.x; ov[i][1] = v.y;
+        }
+      }
+    }
+    float Mc = M;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) Mc = fmaxf(Mc, mv[i]);
+    const float r = ex2(M - Mc);                              // rescale what was merged so far
+    L *= r;
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] *= r;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      if (!use[i]) continue;
+      const float w = ex2(mv[i] - Mc);
+      L += w * lv[i];
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] += w * ov[i][k];
+    }
+    M = Mc;
+  }
+}
+
+// Wide reduce when the grid's pieces per segment reach this many (two chunks of the CTA).
+constexpr int kWideReducePieces = 16;
+
+template <int D, bool WIDE>
 __global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
   constexpr int V = D / 32;                                   // channels per lane
   static_assert(kInlinePlanSeqs == 8 * 32, "one sequence per thread of the CTA");
   __shared__ int snb[kInlinePlanSeqs], spre[kInlinePlanSeqs], schunk[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + warp;
+  const int row = WIDE ? blockIdx.x : blockIdx.x * 8 + warp;
   if (a.inline_plan) {
     // blocks of every sequence and their exclusive prefix: thread t takes sequence t
     const int sq = threadIdx.x;
@@ -231,83 +294,82 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
   }
   grid_dep_wait();
   if (nb > 0 && p0 == p1) return;                             // finished by the attention kernel
+  // Every piece from p0 to p1 holds part of the segment (pieces hold at least 8 positions,
+  // so none is empty) and wrote a state.
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  if (nb > 0) {
-    // Every piece from p0 to p1 holds part of the segment (pieces hold at least 8 positions,
-    // so none is empty) and wrote a state.  Parts are merged in chunks of CH with every load
-    // of a chunk issued before any is used (one memory round trip per chunk instead of one
-    // per part), online across chunks.
-    constexpr int CH = 8;
-    float M = -INFINITY, L = 0.f;
-    for (int pc = p0; pc <= p1; pc += CH) {
-      float mv[CH], lv[CH], ov[CH][V];
-      bool use[CH];
-#pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        const int p = pc + i;
-        use[i] = p <= p1;
-        mv[i] = -INFINITY;
-        lv[i] = 0.f;
-#pragma unroll
-        for (int k = 0; k < V; ++k) ov[i][k] = 0.f;
-        if (use[i]) {
-          const long long part = (seg + p) * a.G + hl;
-          const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + part * 2);
-          mv[i] = ml.x;
-          lv[i] = ml.y;
-          const float* src = a.ws_o + part * D + lane * V;
-          if constexpr (V == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            ov[i][0] = v.x; ov[i][1] = v.y; ov[i][2] = v.z; ov[i][3] = v.w;
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            ov[i][0] = v.x; ov[i][1] = v.y;
-          }
-        }
-      }
-      float Mc = M;
-#pragma unroll
-      for (int i = 0; i < CH; ++i) Mc = fmaxf(Mc, mv[i]);
-      const float r = ex2(M - Mc);                            // rescale what was merged so far
-      L *= r;
-#pragma unroll
-      for (int k = 0; k < V; ++k) acc[k] *= r;
-#pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        if (!use[i]) continue;
-        const float w = ex2(mv[i] - Mc);
-        L += w * lv[i];
-#pragma unroll
-        for (int k = 0; k < V; ++k) acc[k] += w * ov[i][k];
-      }
-      M = Mc;
+  float M = -INFINITY, L = 0.f;
+  if constexpr (WIDE) {
+    __shared__ float sM[8], sL[8];
+    __shared__ __align__(16) float sacc[8][D];
+    if (nb > 0) merge_pieces<D>(a, seg, hl, lane, p0 + warp * kMergeChunk, p1, 8 * kMergeChunk, M, L, acc);
+    if constexpr (V == 4)
+      *reinterpret_cast<float4*>(&sacc[warp][lane * V]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else
+      *reinterpret_cast<float2*>(&sacc[warp][lane * V]) = make_float2(acc[0], acc[1]);
+    if (lane == 0) {
+      sM[warp] = M;
+      sL[warp] = L;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __syncthreads();
+    // thread t < D/2 combines channels 2t, 2t+1 over the warps; warp 0 took p0, so the
+    // largest exponent is finite and warps without pieces weigh zero
+    const int t = threadIdx.x;
+    if (t >= D / 2) return;
+    float o0 = 0.f, o1 = 0.f;
+    if (nb > 0) {
+      float Mt = sM[0];
 #pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] *= inv;
-  }
-  const size_t o = (size_t)row * D + lane * V;
-  if (a.out_f32) {
-    float* out = reinterpret_cast<float*>(a.out) + o;
+      for (int w = 1; w < 8; ++w) Mt = fmaxf(Mt, sM[w]);
+      float Lt = 0.f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) out[i] = acc[i];
+      for (int w = 0; w < 8; ++w) {
+        const float f = ex2(sM[w] - Mt);
+        Lt += f * sL[w];
+        o0 += f * sacc[w][2 * t];
+        o1 += f * sacc[w][2 * t + 1];
+      }
+      const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+      o0 *= inv;
+      o1 *= inv;
+    }
+    const size_t o = (size_t)row * D + 2 * t;
+    if (a.out_f32) {
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + o) = make_float2(o0, o1);
+    } else {
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + o) = pack_bf16(o0, o1);
+    }
   } else {
-    uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + o);
+    if (nb > 0) {
+      merge_pieces<D>(a, seg, hl, lane, p0, p1, kMergeChunk, M, L, acc);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-    for (int i = 0; i < V / 2; ++i) out[i] = pack_bf16(acc[2 * i], acc[2 * i + 1]);
+      for (int i = 0; i < V; ++i) acc[i] *= inv;
+    }
+    const size_t o = (size_t)row * D + lane * V;
+    if (a.out_f32) {
+      float* out = reinterpret_cast<float*>(a.out) + o;
+#pragma unroll
+      for (int i = 0; i < V; ++i) out[i] = acc[i];
+    } else {
+      uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + o);
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) out[i] = pack_bf16(acc[2 * i], acc[2 * i + 1]);
+    }
   }
 }
 
 cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream) {
   const int rows = a.batch * a.n_h;
   if (rows == 0) return cudaSuccess;
-  dim3 grid((rows + 7) / 8), block(256);
+  // the grid's pieces over the segments: about the average a segment spans
+  const bool wide = (long long)P >= (long long)kWideReducePieces * a.batch * a.n_kv;
+  dim3 grid(wide ? rows : (rows + 7) / 8), block(256);
   DecodeArgs args = a;
-  (void)P;
   void* kargs[] = {&args};
-  const void* fn = head_dim == 128 ? (const void*)reduce_kernel<128> : (const void*)reduce_kernel<64>;
+  const void* fn = head_dim == 128 ? (wide ? (const void*)reduce_kernel<128, true> : (const void*)reduce_kernel<128, false>)
+                                   : (wide ? (const void*)reduce_kernel<64, true> : (const void*)reduce_kernel<64, false>);
   return launch_pdl(fn, grid, block, 0, stream, kargs);
 }
 
