@@ -173,22 +173,40 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int max_ctx, int
 // per thread); the context lengths are inputs of the call, and the plan kernel's prefix sums
 // finished before the attention kernel let this one launch.
 //
-// Two shapes.  Narrow: one warp per (sequence, q head), eight rows per CTA, for batches whose
-// segments span few pieces.  Wide: one CTA per row whose eight warps take interleaved chunks
-// of its pieces and combine their eight states through shared memory, for few long
-// sequences, where a segment spans a large share of the grid's pieces and one warp would
-// take one memory round trip per eight of them.
+// Two shapes.  Narrow, for batches whose segments span few pieces: LPR lanes per (sequence,
+// q head) row -- a warp (8 rows per CTA), or half of one (16 rows per CTA, with half the loads
+// per round) when a warp per row would take more CTAs than are resident at once.  Wide: one
+// CTA per row whose eight warps take interleaved chunks of its pieces and combine their
+// eight states through shared memory, for few long sequences, where a segment spans a large
+// share of the grid's pieces and one warp would take one memory round trip per eight of them.
 
-// Pieces one warp loads at a time in merge_pieces.
+// Partial states a warp loads at a time in merge_pieces (LPR = 32 lanes per row: 8 per
+// row; LPR = 16: 4 per row, two rows per warp).
 constexpr int kMergeChunk = 8;
 
+// Vector of V consecutive floats at src (V = 2, 4 or 8; 8-byte aligned, 16 for V >= 4).
+template <int V>
+__device__ __forceinline__ void load_vec(const float* src, float (&v)[V]) {
+  if constexpr (V == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(src);
+    v[0] = x.x; v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < V / 4; ++j) {
+      const float4 x = *reinterpret_cast<const float4*>(src + 4 * j);
+      v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+    }
+  }
+}
+
 // Merges the states of pieces first, first+1, ... (chunks of CH taken every `step` pieces,
-// none past p1) of one (segment, head) into the running (M, L, acc), base-2 exponents.  Every
-// load of a chunk is issued before any is used, and chunks merge online.
-template <int D>
-__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, long long seg, int hl, int lane, int first,
-                                             int p1, int step, float& M, float& L, float (&acc)[D / 32]) {
-  constexpr int V = D / 32, CH = kMergeChunk;
+// none past p1) of one (segment, head) into the running (M, L, acc), base-2 exponents; the
+// LPR lanes of the row hold V = D / LPR channels each (sub: the lane's place).  Every load of
+// a chunk is issued before any is used, and chunks merge online.
+template <int D, int LPR>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, long long seg, int hl, int sub, int first,
+                                             int p1, int step, float& M, float& L, float (&acc)[D / LPR]) {
+  constexpr int V = D / LPR, CH = kMergeChunk * LPR / 32;
   for (int pc = first; pc <= p1; pc += step) {
     float mv[CH], lv[CH], ov[CH][V];
     bool use[CH];
@@ -205,14 +223,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, long long seg,
         const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + part * 2);
         mv[i] = ml.x;
         lv[i] = ml.y;
-        const float* src = a.ws_o + part * D + lane * V;
-        if constexpr (V == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          ov[i][0] = v.x; ov[i][1] = v.y; ov[i][2] = v.z; ov[i][3] = v.w;
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(src);
-          ov[i][0] = v.x; ov[i][1] = v.y;
-        }
+        load_vec<V>(a.ws_o + part * D + sub * V, ov[i]);
       }
     }
     float Mc = M;
@@ -237,13 +248,15 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, long long seg,
 // Wide reduce when the grid's pieces per segment reach this many (two chunks of the CTA).
 constexpr int kWideReducePieces = 16;
 
-template <int D, bool WIDE>
-__global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
-  constexpr int V = D / 32;                                   // channels per lane
+template <int D, bool WIDE, int LPR>
+__global__ void __launch_bounds__(256, LPR == 16 ? 4 : 0) reduce_kernel(const DecodeArgs a) {
+  constexpr int V = D / LPR;                                  // channels per lane
+  constexpr int RPC = 256 / LPR;                              // rows per CTA (narrow)
   static_assert(kInlinePlanSeqs == 8 * 32, "one sequence per thread of the CTA");
+  static_assert(!WIDE || LPR == 32, "a wide CTA's warps each take the whole row");
   __shared__ int snb[kInlinePlanSeqs], spre[kInlinePlanSeqs], schunk[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = WIDE ? blockIdx.x : blockIdx.x * 8 + warp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = threadIdx.x % LPR;
+  const int row = WIDE ? blockIdx.x : blockIdx.x * RPC + threadIdx.x / LPR;
   if (a.inline_plan) {
     // blocks of every sequence and their exclusive prefix: thread t takes sequence t
     const int sq = threadIdx.x;
@@ -303,7 +316,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
   if constexpr (WIDE) {
     __shared__ float sM[8], sL[8];
     __shared__ __align__(16) float sacc[8][D];
-    if (nb > 0) merge_pieces<D>(a, seg, hl, lane, p0 + warp * kMergeChunk, p1, 8 * kMergeChunk, M, L, acc);
+    if (nb > 0) merge_pieces<D, 32>(a, seg, hl, lane, p0 + warp * kMergeChunk, p1, 8 * kMergeChunk, M, L, acc);
     if constexpr (V == 4)
       *reinterpret_cast<float4*>(&sacc[warp][lane * V]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     else
@@ -342,12 +355,13 @@ __global__ void __launch_bounds__(256) reduce_kernel(const DecodeArgs a) {
     }
   } else {
     if (nb > 0) {
-      merge_pieces<D>(a, seg, hl, lane, p0, p1, kMergeChunk, M, L, acc);
+      constexpr int CH = kMergeChunk * LPR / 32;
+      merge_pieces<D, LPR>(a, seg, hl, sub, p0, p1, CH, M, L, acc);
       const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] *= inv;
     }
-    const size_t o = (size_t)row * D + lane * V;
+    const size_t o = (size_t)row * D + sub * V;
     if (a.out_f32) {
       float* out = reinterpret_cast<float*>(a.out) + o;
 #pragma unroll
@@ -365,11 +379,27 @@ cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t
   if (rows == 0) return cudaSuccess;
   // the grid's pieces over the segments: about the average a segment spans
   const bool wide = (long long)P >= (long long)kWideReducePieces * a.batch * a.n_kv;
-  dim3 grid(wide ? rows : (rows + 7) / 8), block(256);
+  // Rows of a warp each, narrow: 16 lanes per row when a warp per row would take more CTAs
+  // than are resident at once (the attention grid holds the SMs until it ends, so the CTAs
+  // past one wave would start only after the first wave's merges).
+  static int wave = 0;
+  if (wave == 0) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reduce_kernel<128, false, 32>, 256, 0) != cudaSuccess)
+      return cudaGetLastError();
+    wave = (occ > 0 ? occ : 1) * (device_sm_count() > 0 ? device_sm_count() : 1);
+  }
+  const bool half = !wide && (rows + 7) / 8 > wave;
+  dim3 grid(wide ? rows : (half ? (rows + 15) / 16 : (rows + 7) / 8)), block(256);
   DecodeArgs args = a;
   void* kargs[] = {&args};
-  const void* fn = head_dim == 128 ? (wide ? (const void*)reduce_kernel<128, true> : (const void*)reduce_kernel<128, false>)
-                                   : (wide ? (const void*)reduce_kernel<64, true> : (const void*)reduce_kernel<64, false>);
+  const void* fn;
+  if (head_dim == 128)
+    fn = wide ? (const void*)reduce_kernel<128, true, 32>
+              : (half ? (const void*)reduce_kernel<128, false, 16> : (const void*)reduce_kernel<128, false, 32>);
+  else
+    fn = wide ? (const void*)reduce_kernel<64, true, 32>
+              : (half ? (const void*)reduce_kernel<64, false, 16> : (const void*)reduce_kernel<64, false, 32>);
   return launch_pdl(fn, grid, block, 0, stream, kargs);
 }
 
