@@ -81,22 +81,25 @@ def test_a_segment_spread_over_hundreds_of_pieces(kernel, monkeypatch):
     assert torch.equal(outs[0], outs[1])
 
 
-def test_long_segment_merges_alike_in_narrow_and_wide_reduce():
-    # The split-reduce takes one warp per row when segments are many, one CTA per row when
-    # few: the same 40 000-token sequence alone (8 segments, the grid's pieces shared among
-    # them) and ahead of 199 short ones (1600 segments, more than the grid has pieces) goes
-    # through the two shapes, each compared with the oracle.
+@pytest.mark.parametrize("D", [64, 128])
+def test_long_segment_merges_alike_in_narrow_and_wide_reduce(D):
+    # The split-reduce takes one CTA per row when segments are few, part of a warp per row
+    # when they are many: the same 40 000-token sequence alone (8 segments, the grid's pieces
+    # shared among them) and ahead of 199 short ones (1600 segments, more than the grid has
+    # pieces; 6400 rows, more than one wave of warp-per-row CTAs, so half a warp per row)
+    # goes through the two shapes, each compared with the oracle, in fp32 and bf16 output.
     BS, n_h, n_kv = 16, 32, 8
-    scale = 1 / math.sqrt(128)
-    q, kp, vp, bt, ctx = _case(200, n_h, n_kv, [40000] + [33 + 5 * i for i in range(199)], BS, seed=21)
+    scale = 1 / math.sqrt(D)
+    q, kp, vp, bt, ctx = _case(200, n_h, n_kv, [40000] + [33 + 5 * i for i in range(199)], BS, seed=21, D=D)
     ref = oracle.paged_decode_attention(f64(q), f64(kp), f64(vp), bt, ctx, scale, BS)
-    ws = torch.full((pkv.decode_workspace_bytes(200, n_h, n_kv, 128, BS),), 0xFF, dtype=torch.uint8,
+    ws = torch.full((pkv.decode_workspace_bytes(200, n_h, n_kv, D, BS),), 0xFF, dtype=torch.uint8,
                     device=DEV)
     for B in (1, 200):
-        err = err_flag()
-        out = torch.full((B, n_h, 128), float("nan"), dtype=torch.float32, device=DEV)
-        pkv.paged_decode_attn(q[:B].to(DEV), kp.to(DEV), vp.to(DEV), torch.as_tensor(bt[:B], device=DEV),
-                              torch.as_tensor(ctx[:B], device=DEV), scale, out=out, workspace=ws, err=err)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        check_attention(out, ref[:B], f"batch {B}")
+        for od in (torch.float32, torch.bfloat16):
+            err = err_flag()
+            out = torch.full((B, n_h, D), float("nan"), dtype=od, device=DEV)
+            pkv.paged_decode_attn(q[:B].to(DEV), kp.to(DEV), vp.to(DEV), torch.as_tensor(bt[:B], device=DEV),
+                                  torch.as_tensor(ctx[:B], device=DEV), scale, out=out, workspace=ws, err=err)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0
+            check_attention(out, ref[:B], f"batch {B} D {D} {od}")
