@@ -374,22 +374,26 @@ __global__ void __launch_bounds__(256, LPR == 16 ? 4 : 0) reduce_kernel(const De
   }
 }
 
+// CTAs of the warp-per-row reduce resident at once on the device (0 if the query failed).
+static int reduce_wave() {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reduce_kernel<128, false, 32>, 256, 0) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return occ * device_sm_count();
+}
+
 cudaError_t launch_reduce(int head_dim, const DecodeArgs& a, int P, cudaStream_t stream) {
   const int rows = a.batch * a.n_h;
   if (rows == 0) return cudaSuccess;
   // the grid's pieces over the segments: about the average a segment spans
   const bool wide = (long long)P >= (long long)kWideReducePieces * a.batch * a.n_kv;
-  // Rows of a warp each, narrow: 16 lanes per row when a warp per row would take more CTAs
-  // than are resident at once (the attention grid holds the SMs until it ends, so the CTAs
-  // past one wave would start only after the first wave's merges).
-  static int wave = 0;
-  if (wave == 0) {
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, reduce_kernel<128, false, 32>, 256, 0) != cudaSuccess)
-      return cudaGetLastError();
-    wave = (occ > 0 ? occ : 1) * (device_sm_count() > 0 ? device_sm_count() : 1);
-  }
-  const bool half = !wide && (rows + 7) / 8 > wave;
+  // Narrow: 16 lanes per row when a warp per row would take more CTAs than are resident at
+  // once (the attention grid holds the SMs until it ends, so the CTAs past one wave would
+  // start only after the first wave's merges).  Either shape gives the same result.
+  static const int wave = reduce_wave();                      // one device per process
+  const bool half = !wide && wave > 0 && (rows + 7) / 8 > wave;
   dim3 grid(wide ? rows : (half ? (rows + 15) / 16 : (rows + 7) / 8)), block(256);
   DecodeArgs args = a;
   void* kargs[] = {&args};
