@@ -115,6 +115,9 @@ size_t pkv_decode_workspace_bytes(int batch, int n_h, int n_kv, int head_dim, in
  * cores (tcgen05.mma, 128-token tiles, accumulators in tensor memory, one CTA per SM);
  * otherwise, and for every other shape, on warp-level mma.sync kernels (several CTAs per
  * SM), which measured faster on that shape.  Same arithmetic and bounds either way.
+ * The first call of a kernel variant on the device sets its shared-memory attribute and
+ * queries occupancy (host-side calls, no stream work); to capture the call into a CUDA
+ * graph, make one call of the same shape on the stream before the capture begins.
  */
 pkv_status pkv_paged_decode_attn(const void* q, const void* k_pool, const void* v_pool,
                                  const int32_t* block_tables, int max_blocks,
