@@ -119,6 +119,35 @@ def test_int4_group_sizes(heads):
     check_attention(out, refo, f"int4 {n_h}/{n_kv}", f32_bars=(BAR_INT4_F32_MAXABS, BAR_INT4_F32_RELL2))
 
 
+def test_long_segment_through_both_reduce_shapes():
+    # One 20 000-token INT4 sequence (8 kv heads) alone -- its segments spread over about 150
+    # pieces each, merged by the one-CTA-per-row reduce -- and ahead of 199 short ones (6400
+    # rows: half a warp per row), both against the oracle.
+    D, BS, n_kv, n_h = 128, 16, 8, 32
+    ctx = np.array([20000] + [33 + 5 * i for i in range(199)], dtype=np.int32)
+    rng = np.random.default_rng(11)
+    bt, num_blocks = _tables(ctx, BS, rng)
+    ks, vs = _history(ctx, n_kv, D, seed=12)
+    cache = pkv.alloc_int4_cache(num_blocks, n_kv, BS, D, len(ctx), DEV)
+    ref = oracle.Int4Cache(num_blocks, n_kv, BS, D, len(ctx))
+    sl = np.concatenate([bt[s, np.arange(c) // BS].astype(np.int64) * BS + np.arange(c) % BS
+                         for s, c in enumerate(ctx)])
+    tl = np.concatenate([np.full(c, s) for s, c in enumerate(ctx)])
+    _append_both(cache, ref, torch.cat(ks), torch.cat(vs), sl, tl)
+    q = torch.randn(len(ctx), n_h, D, generator=torch.Generator().manual_seed(13)).to(torch.bfloat16)
+    scale = 1 / math.sqrt(D)
+    refo = oracle.paged_decode_attention_int4(f64(q), ref, bt, ctx, scale)
+    for B in (1, len(ctx)):
+        err = err_flag()
+        out = pkv.paged_decode_attn_int4(q[:B].to(DEV), cache, torch.as_tensor(bt[:B], device=DEV),
+                                         torch.as_tensor(ctx[:B], device=DEV), scale, out_dtype=torch.float32,
+                                         err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        check_attention(out, refo[:B], f"int4 long segment, batch {B}",
+                        f32_bars=(BAR_INT4_F32_MAXABS, BAR_INT4_F32_RELL2))
+
+
 def test_bad_tail_row_flagged():
     cache = pkv.alloc_int4_cache(4, 1, 16, 64, 2, DEV)
     k = torch.ones(1, 1, 64, dtype=torch.bfloat16, device=DEV)
